@@ -1,0 +1,255 @@
+"""Pins for the oracle's acceptance rules (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy.special import softmax
+
+from oracle import verify as ov
+from oracle.philox import PURPOSE_ACCEPT, PURPOSE_EMIT
+
+
+def test_figure_01_window(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "fig01_window.json")))
+    vid = {w: i for i, w in enumerate(g["vocab"])}
+    res = ov.verify_window(np.float32(g["logits"]), [vid[w] for w in g["drafts"]],
+                           hist=[vid[w] for w in g["emitted_so_far"]], pol=ov.Policy())
+    assert [g["vocab"][t] for t in res.emitted] == g["expected_emitted"]
+    assert res.accept == g["expected_accept"]
+
+
+def _logits_with_argmax(argmax, V, rng):
+    x = rng.standard_normal((len(argmax), V)).astype(np.float32)
+    for r, t in enumerate(argmax):
+        x[r, t] = x[r].max() + 1.0
+    return x
+
+
+def test_greedy_accepts_the_targets_own_chain():
+    rng = np.random.default_rng(0)
+    for k in range(0, 9):
+        am = list(rng.integers(0, 50, k + 1))
+        res = ov.verify_window(_logits_with_argmax(am, 50, rng), am[:k], pol=ov.Policy())
+        assert res.accept == k and res.n_emitted == k + 1 and res.emitted == am
+
+
+def test_greedy_stops_at_the_first_mismatch():
+    rng = np.random.default_rng(1)
+    am = [4, 7, 9, 11]
+    drafts = [4, 7, 3]                      # row 2 perturbed
+    res = ov.verify_window(_logits_with_argmax(am, 20, rng), drafts, pol=ov.Policy())
+    assert res.accept == 2 and res.n_emitted == 3 and res.emitted == [4, 7, 9]
+
+
+def _brute_force_tree(argmax, tokens, parent):
+    """Longest agreeing branch, by walking every node's ancestor path."""
+    best, best_depth = -1, 0
+    for j in range(len(tokens)):
+        path, ok, node = [], True, j
+        while node >= 0:
+            p = parent[node]
+            prow = 0 if p < 0 else 1 + p
+            ok &= tokens[node] == argmax[prow]
+            path.append(node)
+            node = p
+        if ok and len(path) > best_depth:
+            best, best_depth = j, len(path)
+    path = []
+    node = best
+    while node >= 0:
+        path.append(tokens[node])
+        node = parent[node]
+    return path[::-1] + [argmax[0 if best < 0 else 1 + best]], best_depth
+
+
+def test_tree_greedy_matches_brute_force():
+    rng = np.random.default_rng(2)
+    for trial in range(3000):
+        n = int(rng.integers(0, 9))
+        parent = [int(rng.integers(-1, j)) if j else -1 for j in range(n)]
+        tokens = [int(t) for t in rng.integers(0, 3, n)]
+        argmax = [int(t) for t in rng.integers(0, 3, n + 1)]
+        assert ov.accept_greedy(argmax, tokens, parent) == _brute_force_tree(argmax, tokens, parent)
+
+
+def test_single_branch_tree_is_the_chain_rule():
+    rng = np.random.default_rng(3)
+    for trial in range(500):
+        k = int(rng.integers(0, 7))
+        drafts = [int(t) for t in rng.integers(0, 2, k)]
+        argmax = [int(t) for t in rng.integers(0, 2, k + 1)]
+        a = next((i for i in range(k) if drafts[i] != argmax[i]), k)
+        emitted, acc = ov.accept_greedy(argmax, drafts, ov.chain_parents(k))
+        assert acc == a and emitted == drafts[:a] + [argmax[a]]
+
+
+def _dist(ids, probs):
+    return ov.RowDist(list(ids), list(probs), float(np.sum(probs)))
+
+
+def test_accept_predicate_is_min_one_p_over_q():
+    p = [_dist([0, 1], [0.3, 0.7]), _dist([0], [1.0])]
+    q = [_dist([0, 1], [0.6, 0.4])]
+    # p(0)/q(0) = 0.5: u1 just below accepts, just above rejects
+    for u1, acc in ((0.4999, 1), (0.5001, 0)):
+        res, a = ov.accept_rejection_chain(p, q, [0], lambda r, k: u1 if k == PURPOSE_ACCEPT else 0.1)
+        assert a == acc
+    # p(1) > q(1): always accepted
+    res, a = ov.accept_rejection_chain(p, q, [1], lambda r, k: 0.999999 if k == PURPOSE_ACCEPT else 0.1)
+    assert a == 1
+    # on rejection the residual (p - q)+ is {1: 0.3}: token 1 whatever u2
+    res, a = ov.accept_rejection_chain(p, q, [0], lambda r, k: 0.9 if k == PURPOSE_ACCEPT else 0.01)
+    assert res == [1] and a == 0
+
+
+class _Need(Exception):
+    def __init__(self, key):
+        self.key = key
+
+
+def _explore(run, breakpoints):
+    """Exact distribution of run(uniforms) over independent uniforms, for a
+    run that is piecewise constant in each uniform with jumps only at the
+    given breakpoints: evaluate at interval midpoints, weight by length."""
+    out = {}
+
+    def go(fixed, weight):
+        def uniforms(row, purpose):
+            key = (row, purpose)
+            if key in fixed:
+                return fixed[key]
+            raise _Need(key)
+        try:
+            result = run(uniforms)
+        except _Need as need:
+            pts = sorted(set([0.0, 1.0] + [b for b in breakpoints(need.key) if 0.0 < b < 1.0]))
+            for lo, hi in zip(pts[:-1], pts[1:]):
+                if hi > lo:
+                    go({**fixed, need.key: 0.5 * (lo + hi)}, weight * (hi - lo))
+            return
+        out[result] = out.get(result, 0.0) + weight
+    go({}, 1.0)
+    return out
+
+
+def _chain_case(V, k, T, seed, qids=None):
+    rng = np.random.default_rng(seed)
+    logits = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    if qids is None:
+        qids = np.stack([rng.permutation(V)[:8] if V >= 8 else
+                         np.concatenate([rng.permutation(V), rng.integers(0, V, 8 - V)])
+                         for _ in range(k)]).astype(np.int64)
+    qlog = (rng.standard_normal((k, 8)) * 2.0).astype(np.float32)
+    return logits, qids, qlog
+
+
+@pytest.mark.parametrize("V,k,T,seed", [(6, 1, 1.0, 10), (6, 2, 0.7, 11), (5, 2, 1.6, 12)])
+def test_rejection_sampling_is_exact_by_enumeration(V, k, T, seed):
+    """Exact law of the emitted tokens, integrated over every draft outcome
+    and every accept / residual / bonus uniform: the first token follows the
+    target softmax of row 0, and the token at depth j, given the window got
+    there, follows the softmax of row j (full pool: p is a plain softmax)."""
+    logits, qids, qlog = _chain_case(V, k, T, seed)
+    pol = ov.Policy(temperature=T, top_k=0)
+    prep = ov.prepare_rows(logits, [0] * k, ov.chain_parents(k), qids, qlog, [], pol)
+    p_ref = [softmax(logits[r].astype(np.float64) / np.float64(np.float32(T))) for r in range(k + 1)]
+    q_ref = []
+    for i in range(k):
+        w = softmax(qlog[i].astype(np.float64) / np.float64(np.float32(T)))
+        q_ref.append(np.bincount(qids[i], weights=w, minlength=V))
+
+    def breakpoints_for(drafts):
+        def bp(key):
+            row, purpose = key
+            if purpose == PURPOSE_ACCEPT:
+                x = drafts[row]
+                return [p_ref[row][x] / q_ref[row][x]] if q_ref[row][x] > 0 else []
+            pts = list(np.cumsum(np.sort(p_ref[row])[::-1]))
+            pd = prep.pdists[row]
+            order = [pd.ids[j] for j in range(pd.m)]
+            pts += list(np.cumsum(p_ref[row][order]))
+            if row < k:
+                r = np.maximum(p_ref[row][order] - q_ref[row][order], 0.0)
+                if r.sum() > 0:
+                    pts += list(np.cumsum(r) / r.sum())
+            return pts
+        return bp
+
+    first = np.zeros(V)
+    reach = np.zeros(k + 1)
+    at_depth = np.zeros((k + 1, V))
+    for drafts in np.ndindex(*([V] * k)):
+        pd = np.prod([q_ref[i][drafts[i]] for i in range(k)]) if k else 1.0
+        if pd == 0.0:
+            continue
+
+        def run(uniforms, drafts=drafts):
+            em, _ = ov.accept_rejection_chain(prep.pdists, prep.qdists, list(drafts), uniforms)
+            return tuple(em)
+        for em, w in _explore(run, breakpoints_for(drafts)).items():
+            first[em[0]] += pd * w
+            for d, t in enumerate(em):
+                reach[d] += pd * w
+                at_depth[d, t] += pd * w
+    assert abs(first.sum() - 1.0) < 1e-12
+    np.testing.assert_allclose(first, p_ref[0], atol=1e-12)
+    for d in range(1, k + 1):
+        if reach[d] > 1e-6:
+            np.testing.assert_allclose(at_depth[d] / reach[d], p_ref[d], atol=1e-10)
+
+
+def test_naive_descent_is_exact_for_a_deterministic_tree():
+    """Sampled token tree: the first token follows p of the root row and the
+    token after a taken child follows that child's row."""
+    rng = np.random.default_rng(20)
+    V, T = 5, 0.9
+    tokens, parent = [0, 1, 2, 3, 4, 1], [-1, -1, 0, 0, 1, 4]
+    logits = rng.standard_normal((7, V)).astype(np.float32)
+    pol = ov.Policy(temperature=T, top_k=0)
+    prep = ov.prepare_rows(logits, tokens, parent, None, None, [], pol)
+    p_ref = [softmax(logits[r].astype(np.float64) / np.float64(np.float32(T))) for r in range(7)]
+
+    def bp(key):
+        row, _ = key
+        pd = prep.pdists[row]
+        return list(np.cumsum(p_ref[row][pd.ids]))
+
+    law = _explore(lambda u: tuple(ov.accept_naive_descent(prep.pdists, tokens, parent, u)[0]), bp)
+    first = np.zeros(V)
+    second_after_0 = np.zeros(V)
+    for em, w in law.items():
+        first[em[0]] += w
+        if em[0] == 0 and len(em) > 1:
+            second_after_0[em[1]] += w
+    np.testing.assert_allclose(first, p_ref[0], atol=1e-12)
+    # token 0 at the root is node 0 (the lowest index); its row is 1
+    np.testing.assert_allclose(second_after_0 / second_after_0.sum(), p_ref[1], atol=1e-12)
+
+
+def test_every_window_emits_at_least_one_token():
+    rng = np.random.default_rng(30)
+    for trial in range(300):
+        V = int(rng.integers(2, 90))
+        n = int(rng.integers(0, 6))
+        chain = trial % 2 == 0
+        parent = ov.chain_parents(n) if chain else [int(rng.integers(-1, j)) if j else -1 for j in range(n)]
+        tokens = list(rng.integers(0, V, n))
+        logits = (rng.standard_normal((n + 1, V)) * 2).astype(np.float32)
+        pol = ov.Policy(temperature=float(rng.choice([0.0, 0.5, 1.0])), top_k=int(rng.integers(-1, 70)),
+                        min_p=float(rng.uniform(0, 0.2)), top_p=float(rng.uniform(0.5, 1.0)),
+                        presence=1.5, window=int(rng.integers(0, 10)))
+        qids = rng.integers(0, V, (n, 8)) if chain else None
+        qlog = rng.standard_normal((n, 8)).astype(np.float32) if chain else None
+        res = ov.verify_window(logits, tokens, parent, qids, qlog, list(rng.integers(0, V, 12)),
+                               pol, seed=trial, position=7)
+        assert 1 <= res.n_emitted <= n + 1 and res.n_emitted == res.accept + 1
+        assert all(0 <= t < V for t in res.emitted)
+
+
+def test_invalid_trees_are_rejected():
+    logits = np.zeros((3, 4), np.float32)
+    with pytest.raises(ValueError):
+        ov.verify_window(logits, [1, 2], [-1, 1])       # parent is not an earlier node
+    with pytest.raises(ValueError):
+        ov.verify_window(logits, [1, 9], [-1, 0])       # token outside the vocabulary
