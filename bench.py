@@ -1,0 +1,373 @@
+"""Benchmark of the verify step on one GB300 (or N replicas).
+
+Workload: the sampled chain -- hidden 4096, vocab 151936, k = 3 drafts
+(4 verify rows), bf16 LM-head weights N(0, 0.02), fp32 activations N(0, 1),
+draft q over 8 candidates drawn from the target top-32 with logit = target
+logit + N(0, 1); temperature 0.7, top-k absent (20), min-p 0.05, top-p 0.95,
+no penalties.  One step = one fused verify window (projection, pool,
+policy, acceptance).  256 distinct windows (seeds 0..255) are resident in
+HBM and cycled; the 1.24 GB weight stream is larger than L2, so no step
+reuses another's weights from cache.
+
+Prints one JSON line (see the repository's benchmark contract).  With
+--impl reference it times the CPU oracle instead (bounded sample).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+V, H, K_DRAFTS = 151936, 4096, 3
+ROWS = K_DRAFTS + 1
+N_WINDOWS = 256
+WEIGHT_BYTES = V * H * 2
+METRIC = "verify windows/s (hidden 4096, V=151936, k+1 rows); HBM GB/s vs 8 TB/s peak"
+WORKLOAD = "sampled chain: hidden 4096, vocab 151936, k=3 (4 rows), T 0.7, top-k 20, min-p 0.05, top-p 0.95"
+POLICY = dict(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95)
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM bytes from a committed ncu summary, valid only while
+    the kernel source is unchanged since it was taken."""
+    path = os.path.join(HERE, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(HERE, rec["source"])
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if digest == rec["sha256"] else None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples taken while the timed region runs."""
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_windows(torch, vb, synth, wd, dev):
+    """N_WINDOWS resident windows: activations, draft candidates and drafts.
+    The target top-32 that the draft recipe needs is taken from a cuBLAS
+    bf16 product (input preparation only, outside any timed region)."""
+    acts = np.stack([synth.activations(ROWS, H, s) for s in range(N_WINDOWS)])
+    A = torch.from_numpy(acts).to(dev)
+    w_bf16 = wd.view(torch.bfloat16)
+    top_ids, top_vals = [], []
+    for s in range(0, N_WINDOWS, 32):
+        a = A[s:s + 32, :K_DRAFTS].reshape(-1, H).to(torch.bfloat16)
+        lg = (a @ w_bf16.T).float()
+        v, i = torch.topk(lg, 32, dim=1)
+        top_ids.append(i.reshape(-1, K_DRAFTS, 32).cpu().numpy())
+        top_vals.append(v.reshape(-1, K_DRAFTS, 32).cpu().numpy())
+    top_ids = np.concatenate(top_ids)
+    top_vals = np.concatenate(top_vals)
+    q_ids, q_log, drafts = [], [], []
+    for s in range(N_WINDOWS):
+        qi, ql = synth.draft_candidates(top_ids[s], top_vals[s], seed=s)
+        slot = synth.draft_choice(ql, POLICY["temperature"], seed=s + 1)
+        q_ids.append(qi)
+        q_log.append(ql)
+        drafts.append(qi[np.arange(K_DRAFTS), slot].astype(np.int32))
+    return dict(act_np=acts, act=A, q_ids_np=np.stack(q_ids), q_log_np=np.stack(q_log),
+                drafts_np=np.stack(drafts), q_ids=torch.from_numpy(np.stack(q_ids)).to(dev),
+                q_log=torch.from_numpy(np.stack(q_log)).to(dev),
+                drafts=torch.from_numpy(np.stack(drafts)).to(dev))
+
+
+def cpu_oracle_windows(W, win, n_windows, threads_note=True):
+    """Time the oracle as it stands on n_windows full windows of the workload."""
+    from oracle import verify as ov
+    pol = ov.Policy(**POLICY)
+    times = []
+    for s in range(n_windows):
+        t0 = time.perf_counter()
+        L = ov.project(W, win["act_np"][s]).astype(np.float32)
+        ov.verify_window(L, win["drafts_np"][s], None, win["q_ids_np"][s], win["q_log_np"][s], (),
+                         pol, s, 4096)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from speculative_decoding_verify_row_gb300 import synth
+    W = synth.weights(V, H)
+    win = {"act_np": np.stack([synth.activations(ROWS, H, s) for s in range(8)])}
+    # the draft recipe needs the target top-32; the reference arm takes it
+    # from the oracle's own projection of each window
+    from oracle import verify as ov
+    q_ids, q_log, drafts = [], [], []
+    for s in range(8):
+        L = ov.project(W, win["act_np"][s]).astype(np.float32)
+        top = [ov.target_pool(L[r]) for r in range(K_DRAFTS)]
+        qi, ql = synth.draft_candidates(np.stack([t[0][:32] for t in top]),
+                                        np.stack([t[1][:32] for t in top]), seed=s)
+        slot = synth.draft_choice(ql, POLICY["temperature"], seed=s + 1)
+        q_ids.append(qi)
+        q_log.append(ql)
+        drafts.append(qi[np.arange(K_DRAFTS), slot].astype(np.int32))
+    win.update(q_ids_np=np.stack(q_ids), q_log_np=np.stack(q_log), drafts_np=np.stack(drafts))
+    warm = min(args.warmup, 1)
+    steps = max(1, min(args.steps, 6))
+    cpu_oracle_windows(W, win, warm)
+    times = cpu_oracle_windows(W, win, steps)
+    value = steps / sum(times)
+    sample = (f"{steps} full oracle windows of the workload (fp64 projection of 4 x 151936 x 4096 "
+              f"+ penalties/pool/policy/acceptance), {warm} warm-up")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "windows/s",
+            "n_gpus": args.gpus, "steps": steps, "steps_requested": args.steps, "warmup": warm,
+            "ms_per_step": 1000.0 * sum(times) / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": value, "unit": "windows/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    from speculative_decoding_verify_row_gb300 import binding as vb, replicas, synth
+    from speculative_decoding_verify_row_gb300 import build as vbuild
+
+    rank, world, local = replicas.init("nccl" if args.gpus > 1 else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    vbuild.build()
+    vb.lib()
+
+    W = synth.weights(V, H)
+    wd = torch.from_numpy(W.view(np.int16)).to(dev)
+    win = make_windows(torch, vb, synth, wd, dev)
+    pol = vb.Policy(**POLICY)
+    logits = torch.empty((ROWS, V), dtype=torch.float32, device=dev)
+    out = torch.empty(ROWS, dtype=torch.int32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    ne = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = vb.workspace(ROWS, H, V, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def window(i, path=vb.VR_PATH_AUTO):
+        s = i % N_WINDOWS
+        vb.verify_window(wd, win["act"][s], win["drafts"][s], pol, s, 4096, logits, out, acc, ne, ws,
+                         q_ids=win["q_ids"][s], q_logits=win["q_log"][s], path=path, stream=stream)
+
+    for i in range(args.warmup):
+        window(i)
+    torch.cuda.synchronize(dev)
+    if vb.device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- timed region: K fused windows ----
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    replicas.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for i in range(args.steps):
+            window(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    replicas.barrier()
+    elapsed_s = e0.elapsed_time(e1) / 1000.0
+    job_s, job_windows = replicas.job_time_and_units(elapsed_s, args.steps,
+                                                     device=dev if args.gpus > 1 else None)
+    value = job_windows / job_s
+    if vb.device_status(ws) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    # ---- stage breakdown: the same windows through the stage entry points,
+    # events between stages on the launching stream ----
+    n_stage = min(args.steps, 2000)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_stage)]
+    pool_ids = torch.empty((ROWS, 64), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)
+    for i in range(n_stage):
+        s = i % N_WINDOWS
+        evs[i][0].record(stream)
+        vb.verify_project(wd, win["act"][s], logits, ws, stream=stream)
+        evs[i][1].record(stream)
+        vb.verify_sample_accept(logits, win["drafts"][s], pol, s, 4096, out, acc, ne, ws,
+                                q_ids=win["q_ids"][s], q_logits=win["q_log"][s], stream=stream)
+        evs[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    proj_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    samp_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    proj_avg_s = statistics.fmean(proj_ms) / 1000.0
+
+    # ---- window cost against rows (projection stage, both paths) ----
+    sweep = {}
+    for path, name in ((vb.VR_PATH_TC, "tc"), (vb.VR_PATH_FFMA, "ffma")):
+        sweep[name] = {}
+        for R in (1, 2, 4, 8, 9, 16, 24, 25, 32):
+            a = torch.from_numpy(synth.activations(R, H, 9000 + R)).to(dev)
+            lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+            wsr = vb.workspace(R, H, V, device=dev)
+            for _ in range(3):
+                vb.verify_project(wd, a, lg, wsr, path=path, stream=stream)
+            n_it = 30
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(n_it):
+                vb.verify_project(wd, a, lg, wsr, path=path, stream=stream)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            sweep[name][str(R)] = round(1000.0 * t0.elapsed_time(t1) / n_it, 2)
+
+    # ---- e2e: host inputs -> window -> host outputs, through the C ABI ----
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    h_act = [pin(win["act_np"][s]) for s in range(N_WINDOWS)]
+    h_dr = [pin(win["drafts_np"][s]) for s in range(N_WINDOWS)]
+    h_qi = [pin(win["q_ids_np"][s]) for s in range(N_WINDOWS)]
+    h_ql = [pin(win["q_log_np"][s]) for s in range(N_WINDOWS)]
+    h_out = pin(np.zeros(ROWS, np.int32))
+    n_e2e = min(args.steps, 2000)
+    for i in range(10):
+        vb.verify_window_host(wd, h_act[i], h_dr[i], pol, i, 4096, logits, h_out, ws,
+                              q_ids_h=h_qi[i], q_logits_h=h_ql[i], stream=stream)
+    replicas.barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        s = i % N_WINDOWS
+        vb.verify_window_host(wd, h_act[s], h_dr[s], pol, s, 4096, logits, h_out, ws,
+                              q_ids_h=h_qi[s], q_logits_h=h_ql[s], stream=stream)
+    e2e_s = time.perf_counter() - t0
+    replicas.barrier()
+    e2e_job_s, e2e_units = replicas.job_time_and_units(e2e_s, n_e2e,
+                                                       device=dev if args.gpus > 1 else None)
+    h2d = ROWS * H * 4 + K_DRAFTS * 4 + K_DRAFTS * 8 * 4 * 2
+    d2h = ROWS * 4 + 2 * 4
+
+    peak, peak_kind = measured_peaks()
+    achieved = WEIGHT_BYTES / proj_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * job_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16xf32->f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "hidden": H, "vocab": V,
+                   "distinct_windows": N_WINDOWS, "l2": "inputs larger than L2 (1.24 GB weights)",
+                   "projection_path": "tc", "parallelism": f"replicas x{world}"},
+        "hbm_gbs": WEIGHT_BYTES * value / world / 1e9,
+        "hbm_frac_of_8tbs": WEIGHT_BYTES * value / world / 8e12,
+        "roofline": {"bound": "hbm", "kernel": "projection (split_planes + project_tc_kernel)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_record("project_tc_kernel"),
+                     "algorithmic_bytes_per_launch": WEIGHT_BYTES},
+        "stages_us": {"projection": 1000.0 * statistics.fmean(proj_ms),
+                      "pool_policy_accept": 1000.0 * statistics.fmean(samp_ms),
+                      "window": 1e6 * job_s / args.steps},
+        "rows_sweep_us": sweep,
+        "clocks": clocks.summary(),
+        "e2e": {"value": e2e_units / e2e_job_s, "unit": "windows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times = cpu_oracle_windows(W, win, 3)
+        line["cpu_baseline"] = {"value": 3 / sum(times), "unit": "windows/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": "3 full oracle windows of the workload (fp64 projection "
+                                          "+ pool/policy/acceptance)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    replicas.shutdown()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,281 @@
+/*
+ * verifyrow -- the data-parallel hot path of the speculative-decoding verify
+ * step, for one NVIDIA GB300 (sm_103a).
+ *
+ * One verify window scores the current position plus the draft tokens in a
+ * single pass ("Speculative decoding on RDNA", §01 figure "one speculative
+ * window": k drafts, k + 1 verify rows), penalises every row against its own
+ * history (§04), turns each row into the sampler's distribution (§03 "how
+ * hipfire does it") and decides how many drafts to keep (§02 greedy, §03
+ * rejection sampling; token trees from "One RDNA4 verify pass has slack for
+ * about two dozen speculative tokens", "Spend the budget on a tree"; naive
+ * sampling verify from "feat(dflash): developer-only online draft tuning",
+ * notes under the spec-step listing).
+ *
+ * Conventions that hold for every entry point below.
+ *   - Array arguments are DEVICE pointers owned by the caller, unless the
+ *     argument is documented as a host pointer.  The library allocates no
+ *     memory: its scratch is the caller's workspace `ws` of `ws_bytes`
+ *     bytes (device memory, 256-byte aligned), sized by vr_workspace_bytes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work
+ *     is enqueued asynchronously; outputs are valid once the stream has
+ *     reached that point.  No entry point synchronises unless it says so.
+ *   - Return value: VR_OK or a negative VR_ERR_* code.  Argument errors are
+ *     detected on the host before anything is enqueued.  Errors that depend
+ *     on device-resident data (a token outside the vocabulary, a parent
+ *     array that is not topological) are recorded in a status word inside
+ *     the workspace and make that window emit nothing (*out_n_emitted = 0);
+ *     read them with vr_device_status.  Nothing traps on the device.
+ *   - Rows and nodes.  A window verifies n_nodes draft nodes over
+ *     rows = n_nodes + 1 rows.  Row 0 scores the current position; row 1+j
+ *     scores the position after node j.  `parent` == NULL means a chain
+ *     (node j hangs from node j-1); otherwise parent[j] is -1 (the root) or
+ *     an earlier node.  Node j is checked against row(parent[j]).
+ *   - Matrices are row-major.  weight: [vocab][hidden] bf16 bit patterns
+ *     (the LM-head layout); act: [rows][hidden] float; logits:
+ *     [rows][vocab] float.
+ */
+#ifndef VERIFYROW_H
+#define VERIFYROW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VR_API __attribute__((visibility("default")))
+#else
+#define VR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VR_ABI_VERSION 1
+
+/* status codes */
+#define VR_OK 0
+#define VR_ERR_ARG (-1)          /* a NULL, a size out of range, bad policy    */
+#define VR_ERR_CUDA (-2)         /* a CUDA call or launch failed               */
+#define VR_ERR_UNSUPPORTED (-3)  /* shape the kernels do not handle            */
+#define VR_ERR_DEVICE (-4)       /* the device status word is set              */
+#define VR_ERR_WORKSPACE (-5)    /* ws is NULL, misaligned or too small        */
+
+/* device status word bits (vr_device_status) */
+#define VR_DEV_BAD_TOKEN 1       /* a draft token outside [0, vocab)           */
+#define VR_DEV_BAD_PARENT 2      /* parent[j] not in [-1, j)                   */
+#define VR_DEV_BAD_QID 4         /* a draft candidate id outside [0, vocab)    */
+#define VR_DEV_TIMEOUT 8         /* a bounded on-chip wait gave up             */
+
+/* projection paths; chosen per weight matrix, never by row count */
+#define VR_PATH_AUTO 0           /* = VR_PATH_TC                               */
+#define VR_PATH_FFMA 1           /* CUDA-core multi-row GEMV (fp32 FMA)        */
+#define VR_PATH_TC 2             /* tcgen05 tensor cores, exact 3-plane split  */
+
+/* limits */
+#define VR_POOL 64               /* pool width ("Speculative decoding on RDNA" §03) */
+#define VR_QCAND 8               /* draft candidates per draft row (same section)   */
+#define VR_MAX_WINDOW_ROWS 64    /* rows of one request (k + 1 or nodes + 1)         */
+#define VR_MAX_ROWS 1024         /* rows of one projection / batched call            */
+#define VR_MAX_PENALTY_WINDOW 512
+#define VR_MAX_REQUESTS 256
+
+/*
+ * Sampler and penalty settings of one request ("Speculative decoding on
+ * RDNA" §03: temperature, top-k with absent = 20 and 0 = the 64-wide pool,
+ * min-p, top-p; §04: repeat, presence and frequency penalties over the last
+ * W tokens).  temperature == 0 means greedy.  Validation (VR_ERR_ARG):
+ * temperature, min_p, top_p finite and temperature >= 0; repeat finite and
+ * > 0; presence, frequency finite; 0 <= window <= VR_MAX_PENALTY_WINDOW.
+ */
+typedef struct vr_policy {
+  float temperature;  /* 0 => greedy                                        */
+  int32_t top_k;      /* < 0 absent => 20; 0 => 64 (whole pool); > 64 => 64 */
+  float min_p;        /* <= 0 disables                                      */
+  float top_p;        /* >= 1 disables                                      */
+  float repeat;       /* 1 disables                                         */
+  float presence;     /* 0 disables                                         */
+  float frequency;    /* 0 disables                                         */
+  int32_t window;     /* W; 0 disables every penalty                        */
+} vr_policy;
+
+/* One request of a batched call (host struct holding device pointers). */
+typedef struct vr_request {
+  int32_t n_nodes;          /* the request owns n_nodes + 1 consecutive rows  */
+  const int32_t* tokens;    /* [n_nodes] draft tokens                         */
+  const int32_t* parent;    /* [n_nodes] or NULL (chain)                      */
+  const int32_t* q_ids;     /* [n_nodes][8] draft candidates or NULL          */
+  const float* q_logits;    /* [n_nodes][8] their logits or NULL              */
+  const int32_t* hist;      /* [hist_len] prompt || emitted so far            */
+  int32_t hist_len;
+  vr_policy policy;
+  uint64_t seed;            /* request seed of the random stream              */
+  uint64_t position;        /* |prompt || emitted| at the window start        */
+  int32_t* out_ids;         /* [n_nodes + 1] emitted ids                      */
+  int32_t* out_accept;      /* [1] accepted drafts                            */
+  int32_t* out_n_emitted;   /* [1] emitted ids (accepted + 1; 0 on error)     */
+} vr_request;
+
+/* ABI version (VR_ABI_VERSION) and a static text for a status code. */
+VR_API int vr_abi_version(void);
+VR_API const char* vr_status_string(int status);
+
+/*
+ * Workspace bytes for a call over `rows` rows (all requests together),
+ * `hidden` and `vocab`.  One workspace may be reused by consecutive calls
+ * on one stream; calls that may overlap need separate workspaces.
+ * Errors: VR_ERR_ARG if out_bytes is NULL or a size is out of range.
+ */
+VR_API int vr_workspace_bytes(int rows, int hidden, int vocab, size_t* out_bytes);
+
+/*
+ * (a1) Multi-row verify projection ("Speculative decoding on RDNA" §01: the
+ * weights are read once for all k + 1 rows; §02: multi-row projections sum
+ * in the single-row order).
+ *   logits[r][v] = sum_h weight[v][h] * act[r][h], fp32 accumulation.
+ * Each weight byte is streamed from HBM once per call for all rows.  For a
+ * given path, hidden and vocab, the bits of row r do not depend on `rows`
+ * or on the other rows' values, so a row computed inside an R-row call is
+ * identical to the same row computed alone.
+ * rows in [1, VR_MAX_ROWS]; hidden a multiple of 8 in [8, 65536];
+ * vocab in [1, 2^31 - 1].  path: VR_PATH_*.  Writes logits only.
+ */
+VR_API int vr_verify_project(const uint16_t* weight, const float* act, int rows, int hidden,
+                      int vocab, int path, float* logits, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * (a2) Per-row penalty prepass, in place ("Speculative decoding on RDNA"
+ * §04): row r is penalised against H_r, the last W tokens of
+ * (hist || tokens on the path root -> node r-1), i.e. for a chain
+ * H_i = last W of (prompt || emitted || drafts[0..i)).  For each distinct
+ * token t of H_r with count c (t outside [0, vocab) is ignored), in float32
+ * operations rounded to nearest:
+ *   x = logits[r][t]; if repeat != 1: x = x > 0 ? x / repeat : x * repeat;
+ *   if frequency != 0: x -= (float)c * frequency; if presence != 0: x -= presence.
+ * If q_logits is non-NULL the same is applied in place to the draft
+ * candidates of node j (q_ids[j][0..8)) with H_row(parent[j]).  A policy with
+ * window == 0 or all three penalties neutral leaves everything untouched.
+ * rows = n_nodes + 1 <= VR_MAX_WINDOW_ROWS.
+ */
+VR_API int vr_verify_penalize(float* logits, int rows, int vocab, const int32_t* tokens,
+                       const int32_t* parent, int n_nodes, const int32_t* hist, int hist_len,
+                       const vr_policy* policy, const int32_t* q_ids, float* q_logits,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * (a3) Candidate pool of every row: the first min(64, vocab) entries of the
+ * row in the order (value descending, token id ascending), where every NaN
+ * ranks below -inf and -0.0 below +0.0 ("Speculative decoding on RDNA" §03:
+ * a 64-wide pool with a fixed tie order).  pool_ids/pool_vals:
+ * [rows][64]; slots past min(64, vocab) get id -1 and value NaN.
+ * pool_vals holds the logits' own bits.  pool_ids[r][0] is the row argmax.
+ */
+VR_API int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids,
+                     float* pool_vals, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * (a4) Sampler policy on given pools ("Speculative decoding on RDNA" §03):
+ * pool_vals [rows][64] in pool order, pool_len valid entries per row.
+ * K = 20 if top_k absent, 64 if 0, else min(top_k, 64), at most pool_len;
+ * greedy (temperature 0) keeps pool[0] alone with weight 1; otherwise
+ * e_0 = 1, e_j = vexp((v_j - v_0) / T) in double (0 for NaN or -inf), then
+ * min-p cuts at the first e_j < min_p, top-p keeps the shortest prefix
+ * whose running sum reaches top_p * sum, and S is the sequential sum.
+ * vexp is a Cody-Waite reduction plus a degree-13 Taylor polynomial in IEEE
+ * double +, -, x only, so results are identical on every IEEE machine.
+ * Outputs: out_m [rows] kept count, out_e [rows][64] (zeros past m),
+ * out_S [rows].
+ */
+VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,
+                     int32_t* out_m, double* out_e, double* out_S, void* stream);
+
+/*
+ * (a3)+(a4)+(a5) Pool, policy and acceptance on already-penalised logits.
+ *   greedy: chain -> the longest prefix of drafts equal to the row argmax,
+ *     then the argmax at the first mismatch or the bonus after the last row
+ *     (§02); tree -> the deepest node whose whole path agrees with the
+ *     argmax of each parent row (equal depths: the lower node index).
+ *   sampled chain with q_ids/q_logits (penalised by the caller):
+ *     rejection sampling (§03): accept d_i iff u1 * q_i(d_i) < p_i(d_i)
+ *     (q_i(d_i) = 0: iff p_i(d_i) > 0); on rejection emit a draw from
+ *     (p_i - q_i)+ renormalised (from p_i if that is all zero) and stop; after
+ *     k acceptances draw the bonus from p_k.  q_i is the same policy on the
+ *     8 candidates of node i ordered like the pool.
+ *   sampled tree, or sampled chain without q: naive sampling descent: from
+ *     the root draw y ~ p(row); move to the lowest-index child carrying y,
+ *     else emit y and stop.
+ * Draws: u = Philox4x64-10(counter = (position, row, purpose, 0),
+ * key = (seed, 0)) word 0 >> 11, times 2^-53; purpose 1 = accept uniform,
+ * 2 = emitted draw; t = u * S picks the first j whose running sum exceeds t.
+ * Outputs: out_ids [n_nodes + 1] (emitted ids, then untouched), out_accept,
+ * out_n_emitted (= accepted + 1 >= 1; 0 if the device status was set).
+ */
+VR_API int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab, const int32_t* tokens,
+                            const int32_t* parent, int n_nodes, const int32_t* q_ids,
+                            const float* q_logits, const vr_policy* policy, uint64_t seed,
+                            uint64_t position, int32_t* out_ids, int32_t* out_accept,
+                            int32_t* out_n_emitted, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole window in one call: projection -> penalties -> pool -> policy ->
+ * acceptance, enqueued on `stream` with no host synchronisation.
+ * logits receives the raw projection.  If the policy has active penalties:
+ * pen_logits (if non-NULL) receives the penalised rows and logits stays raw;
+ * if pen_logits is NULL, logits is penalised in place.  q_logits is read
+ * only (its penalised copy lives in ws).  Semantics as in the calls above.
+ */
+VR_API int vr_verify_window(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
+                     int path, const int32_t* tokens, const int32_t* parent, int n_nodes,
+                     const int32_t* q_ids, const float* q_logits, const int32_t* hist,
+                     int hist_len, const vr_policy* policy, uint64_t seed, uint64_t position,
+                     float* logits, float* pen_logits, int32_t* out_ids, int32_t* out_accept,
+                     int32_t* out_n_emitted, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Many independent requests in one call: their rows are stacked in `act`
+ * (request b owns n_nodes_b + 1 consecutive rows, in the order of `reqs`)
+ * and share one projection; penalties, pools, policies and acceptance run
+ * per request with that request's policy, seed, position and history.
+ * `reqs` is a HOST array of n_req descriptors (copied into ws before the call
+ * returns).  total rows <= VR_MAX_ROWS, n_req <= VR_MAX_REQUESTS.
+ * logits/pen_logits as in vr_verify_window.
+ */
+VR_API int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidden, int vocab,
+                             int path, const vr_request* reqs, int n_req, float* logits,
+                             float* pen_logits, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * vr_verify_window with HOST inputs and outputs, for callers whose per-window
+ * data lives on the host: act_h [rows][hidden], tokens_h, parent_h (or
+ * NULL), q_ids_h/q_logits_h (or NULL), hist_h [hist_len] are host pointers
+ * (pinned memory makes the copies asynchronous); the last
+ * min(hist_len, VR_MAX_PENALTY_WINDOW) history tokens are copied.  weight,
+ * logits and pen_logits are device pointers.  The call copies the inputs
+ * into ws, runs the window, copies out_ids_h [rows], *out_accept_h and
+ * *out_n_emitted_h back and SYNCHRONISES the stream before returning.
+ */
+VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
+                          int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,
+                          int n_nodes, const int32_t* q_ids_h, const float* q_logits_h,
+                          const int32_t* hist_h, int hist_len, const vr_policy* policy,
+                          uint64_t seed, uint64_t position, float* logits, float* pen_logits,
+                          int32_t* out_ids_h, int32_t* out_accept_h, int32_t* out_n_emitted_h,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Read and clear the device status word of a workspace (VR_DEV_* bits).
+ * Synchronises `stream`.  Returns VR_OK, or VR_ERR_CUDA.
+ */
+VR_API int vr_device_status(void* ws, int32_t* out_status, void* stream);
+
+/*
+ * Zero-initialise a fresh workspace (the status word).  Call once after
+ * allocating ws; enqueued on `stream`.
+ */
+VR_API int vr_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VERIFYROW_H */

@@ -1,0 +1,344 @@
+"""Thin Python binding of libverifyrow (argument marshalling only).
+
+Every function here checks tensor devices, dtypes and shapes, passes raw
+pointers and sizes to the C ABI declared in include/verifyrow.h, and turns a
+negative status into VerifyRowError.  All computation happens in the CUDA
+kernels behind the C ABI; there is no fallback: if the shared library is
+missing or fails to load, every call raises.
+
+Device tensors are torch CUDA tensors; the stream is the current torch
+stream of the tensors' device unless one is given.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libverifyrow.so")
+
+VR_OK = 0
+VR_ERR_ARG = -1
+VR_ERR_CUDA = -2
+VR_ERR_UNSUPPORTED = -3
+VR_ERR_DEVICE = -4
+VR_ERR_WORKSPACE = -5
+VR_DEV_BAD_TOKEN = 1
+VR_DEV_BAD_PARENT = 2
+VR_DEV_BAD_QID = 4
+VR_DEV_TIMEOUT = 8
+VR_PATH_AUTO = 0
+VR_PATH_FFMA = 1
+VR_PATH_TC = 2
+VR_POOL = 64
+VR_QCAND = 8
+VR_MAX_WINDOW_ROWS = 64
+VR_MAX_ROWS = 1024
+VR_MAX_PENALTY_WINDOW = 512
+VR_MAX_REQUESTS = 256
+
+
+class VerifyRowError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().vr_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: {msg} ({status})")
+
+
+class vr_policy(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32),
+                ("min_p", ctypes.c_float), ("top_p", ctypes.c_float),
+                ("repeat", ctypes.c_float), ("presence", ctypes.c_float),
+                ("frequency", ctypes.c_float), ("window", ctypes.c_int32)]
+
+
+class vr_request(ctypes.Structure):
+    _fields_ = [("n_nodes", ctypes.c_int32), ("tokens", ctypes.c_void_p),
+                ("parent", ctypes.c_void_p), ("q_ids", ctypes.c_void_p),
+                ("q_logits", ctypes.c_void_p), ("hist", ctypes.c_void_p),
+                ("hist_len", ctypes.c_int32), ("policy", vr_policy),
+                ("seed", ctypes.c_uint64), ("position", ctypes.c_uint64),
+                ("out_ids", ctypes.c_void_p), ("out_accept", ctypes.c_void_p),
+                ("out_n_emitted", ctypes.c_void_p)]
+
+
+@dataclass
+class Policy:
+    """Sampler and penalty settings of one request (mirrors vr_policy)."""
+    temperature: float = 0.0
+    top_k: int = -1
+    min_p: float = 0.0
+    top_p: float = 1.0
+    repeat: float = 1.0
+    presence: float = 0.0
+    frequency: float = 0.0
+    window: int = 0
+
+    def c(self):
+        return vr_policy(self.temperature, self.top_k, self.min_p, self.top_p, self.repeat,
+                         self.presence, self.frequency, self.window)
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_U64 = ctypes.c_uint64
+
+_SIGNATURES = {
+    "vr_abi_version": ([], _I),
+    "vr_status_string": ([_I], ctypes.c_char_p),
+    "vr_workspace_bytes": ([_I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "vr_workspace_init": ([_P, _SZ, _P], _I),
+    "vr_verify_project": ([_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "vr_verify_penalize": ([_P, _I, _I, _P, _P, _I, _P, _I, ctypes.POINTER(vr_policy), _P, _P,
+                            _P, _SZ, _P], _I),
+    "vr_verify_select": ([_P, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "vr_verify_policy": ([_P, _I, _I, ctypes.POINTER(vr_policy), _P, _P, _P, _P], _I),
+    "vr_verify_sample_accept": ([_P, _I, _I, _P, _P, _I, _P, _P, ctypes.POINTER(vr_policy),
+                                 _U64, _U64, _P, _P, _P, _P, _SZ, _P], _I),
+    "vr_verify_window": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I,
+                          ctypes.POINTER(vr_policy), _U64, _U64, _P, _P, _P, _P, _P, _P, _SZ,
+                          _P], _I),
+    "vr_verify_window_batched": ([_P, _P, _I, _I, _I, ctypes.POINTER(vr_request), _I, _P, _P,
+                                  _P, _SZ, _P], _I),
+    "vr_verify_window_host": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I,
+                               ctypes.POINTER(vr_policy), _U64, _U64, _P, _P, _P, _P, _P, _P,
+                               _SZ, _P], _I),
+    "vr_device_status": ([_P, ctypes.POINTER(ctypes.c_int32), _P], _I),
+}
+
+
+def lib():
+    """Load libverifyrow.so (built by __graft_entry__.build() or build.py)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libverifyrow.so is not built ({LIB_PATH}); run the build step")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = handle
+    return _LIB
+
+
+def _check(status, where):
+    if status != VR_OK:
+        raise VerifyRowError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name, shape=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream(stream, device=None):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_WEIGHT_DTYPES = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def workspace_bytes(rows, hidden, vocab):
+    out = _SZ(0)
+    _check(lib().vr_workspace_bytes(rows, hidden, vocab, ctypes.byref(out)), "vr_workspace_bytes")
+    return out.value
+
+
+def workspace(rows, hidden, vocab, device="cuda", stream=None):
+    """Allocate (through torch) and initialise a workspace for these sizes."""
+    n = workspace_bytes(rows, hidden, vocab)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    _check(lib().vr_workspace_init(_ptr(ws), n, _stream(stream, ws.device)), "vr_workspace_init")
+    return ws
+
+
+def device_status(ws, stream=None):
+    out = ctypes.c_int32(0)
+    _check(lib().vr_device_status(_ptr(ws), ctypes.byref(out), _stream(stream, ws.device)),
+           "vr_device_status")
+    return out.value
+
+
+def verify_project(weight, act, logits, ws, path=VR_PATH_AUTO, stream=None):
+    V, H = weight.shape
+    R = act.shape[0]
+    _dev(weight, _WEIGHT_DTYPES, "weight")
+    _dev(act, torch.float32, "act", (R, H))
+    _dev(logits, torch.float32, "logits", (R, V))
+    _check(lib().vr_verify_project(_ptr(weight), _ptr(act), R, H, V, path, _ptr(logits), _ptr(ws),
+                                   ws.numel(), _stream(stream, act.device)), "vr_verify_project")
+    return logits
+
+
+def _opt_i32(t, name, shape=None):
+    _dev(t, torch.int32, name, shape)
+    return _ptr(t)
+
+
+def verify_penalize(logits, tokens, hist, policy, ws, parent=None, q_ids=None, q_logits=None,
+                    stream=None):
+    R, V = logits.shape
+    n = R - 1
+    _dev(logits, torch.float32, "logits")
+    _dev(q_logits, torch.float32, "q_logits", (n, VR_QCAND))
+    pol = policy.c()
+    _check(lib().vr_verify_penalize(_ptr(logits), R, V, _opt_i32(tokens, "tokens", (n,)),
+                                    _opt_i32(parent, "parent", (n,)), n,
+                                    _opt_i32(hist, "hist"), 0 if hist is None else hist.numel(),
+                                    ctypes.byref(pol), _opt_i32(q_ids, "q_ids", (n, VR_QCAND)),
+                                    _ptr(q_logits), _ptr(ws), ws.numel(),
+                                    _stream(stream, logits.device)), "vr_verify_penalize")
+    return logits
+
+
+def verify_select(logits, pool_ids, pool_vals, ws, stream=None):
+    R, V = logits.shape
+    _dev(logits, torch.float32, "logits")
+    _dev(pool_ids, torch.int32, "pool_ids", (R, VR_POOL))
+    _dev(pool_vals, torch.float32, "pool_vals", (R, VR_POOL))
+    _check(lib().vr_verify_select(_ptr(logits), R, V, _ptr(pool_ids), _ptr(pool_vals), _ptr(ws),
+                                  ws.numel(), _stream(stream, logits.device)), "vr_verify_select")
+    return pool_ids, pool_vals
+
+
+def verify_policy(pool_vals, pool_len, policy, out_m, out_e, out_S, stream=None):
+    R = pool_vals.shape[0]
+    _dev(pool_vals, torch.float32, "pool_vals", (R, VR_POOL))
+    _dev(out_m, torch.int32, "out_m", (R,))
+    _dev(out_e, torch.float64, "out_e", (R, VR_POOL))
+    _dev(out_S, torch.float64, "out_S", (R,))
+    pol = policy.c()
+    _check(lib().vr_verify_policy(_ptr(pool_vals), R, pool_len, ctypes.byref(pol), _ptr(out_m),
+                                  _ptr(out_e), _ptr(out_S), _stream(stream, pool_vals.device)),
+           "vr_verify_policy")
+
+
+def verify_sample_accept(pen_logits, tokens, policy, seed, position, out_ids, out_accept,
+                         out_n, ws, parent=None, q_ids=None, q_logits=None, stream=None):
+    R, V = pen_logits.shape
+    n = R - 1
+    _dev(pen_logits, torch.float32, "pen_logits")
+    _dev(q_logits, torch.float32, "q_logits", (n, VR_QCAND))
+    _dev(out_ids, torch.int32, "out_ids", (R,))
+    _dev(out_accept, torch.int32, "out_accept", (1,))
+    _dev(out_n, torch.int32, "out_n", (1,))
+    pol = policy.c()
+    _check(lib().vr_verify_sample_accept(_ptr(pen_logits), R, V, _opt_i32(tokens, "tokens", (n,)),
+                                         _opt_i32(parent, "parent", (n,)), n,
+                                         _opt_i32(q_ids, "q_ids", (n, VR_QCAND)), _ptr(q_logits),
+                                         ctypes.byref(pol), seed, position, _ptr(out_ids),
+                                         _ptr(out_accept), _ptr(out_n), _ptr(ws), ws.numel(),
+                                         _stream(stream, pen_logits.device)),
+           "vr_verify_sample_accept")
+
+
+def verify_window(weight, act, tokens, policy, seed, position, logits, out_ids, out_accept,
+                  out_n, ws, parent=None, q_ids=None, q_logits=None, hist=None, pen_logits=None,
+                  path=VR_PATH_AUTO, stream=None):
+    V, H = weight.shape
+    R = act.shape[0]
+    n = R - 1
+    _dev(weight, _WEIGHT_DTYPES, "weight")
+    _dev(act, torch.float32, "act", (R, H))
+    _dev(logits, torch.float32, "logits", (R, V))
+    _dev(pen_logits, torch.float32, "pen_logits", (R, V))
+    _dev(q_logits, torch.float32, "q_logits", (n, VR_QCAND))
+    _dev(out_ids, torch.int32, "out_ids", (R,))
+    _dev(out_accept, torch.int32, "out_accept", (1,))
+    _dev(out_n, torch.int32, "out_n", (1,))
+    pol = policy.c()
+    _check(lib().vr_verify_window(_ptr(weight), _ptr(act), R, H, V, path,
+                                  _opt_i32(tokens, "tokens", (n,)), _opt_i32(parent, "parent", (n,)),
+                                  n, _opt_i32(q_ids, "q_ids", (n, VR_QCAND)), _ptr(q_logits),
+                                  _opt_i32(hist, "hist"), 0 if hist is None else hist.numel(),
+                                  ctypes.byref(pol), seed, position, _ptr(logits),
+                                  _ptr(pen_logits), _ptr(out_ids), _ptr(out_accept), _ptr(out_n),
+                                  _ptr(ws), ws.numel(), _stream(stream, act.device)),
+           "vr_verify_window")
+
+
+def make_request(n_nodes, tokens, policy, seed, position, out_ids, out_accept, out_n,
+                 parent=None, q_ids=None, q_logits=None, hist=None):
+    """A vr_request descriptor over device tensors (the tensors must outlive the call)."""
+    for t, name, dt in ((tokens, "tokens", torch.int32), (parent, "parent", torch.int32),
+                        (q_ids, "q_ids", torch.int32), (q_logits, "q_logits", torch.float32),
+                        (hist, "hist", torch.int32), (out_ids, "out_ids", torch.int32),
+                        (out_accept, "out_accept", torch.int32), (out_n, "out_n", torch.int32)):
+        _dev(t, dt, name)
+    return vr_request(n_nodes, _ptr(tokens), _ptr(parent), _ptr(q_ids), _ptr(q_logits),
+                      _ptr(hist), 0 if hist is None else hist.numel(), policy.c(), seed, position,
+                      _ptr(out_ids), _ptr(out_accept), _ptr(out_n))
+
+
+def verify_window_batched(weight, act, requests, logits, ws, pen_logits=None, path=VR_PATH_AUTO,
+                          stream=None):
+    V, H = weight.shape
+    R = act.shape[0]
+    _dev(weight, _WEIGHT_DTYPES, "weight")
+    _dev(act, torch.float32, "act", (R, H))
+    _dev(logits, torch.float32, "logits", (R, V))
+    _dev(pen_logits, torch.float32, "pen_logits", (R, V))
+    arr = (vr_request * len(requests))(*requests)
+    _check(lib().vr_verify_window_batched(_ptr(weight), _ptr(act), H, V, path, arr, len(requests),
+                                          _ptr(logits), _ptr(pen_logits), _ptr(ws), ws.numel(),
+                                          _stream(stream, act.device)),
+           "vr_verify_window_batched")
+
+
+def _host_ptr(a, dtype, name):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or a.dtype != dtype or not a.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous host tensor of {dtype}")
+        return ctypes.c_void_p(a.data_ptr())
+    raise TypeError(f"{name} must be a host torch tensor")
+
+
+def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
+                       ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
+                       pen_logits=None, path=VR_PATH_AUTO, stream=None):
+    """The window with host inputs and outputs (pinned host tensors make the
+    copies asynchronous).  Returns (accept, n_emitted); synchronises."""
+    V, H = weight.shape
+    R = act_h.shape[0]
+    n = R - 1
+    _dev(weight, _WEIGHT_DTYPES, "weight")
+    _dev(logits, torch.float32, "logits", (R, V))
+    _dev(pen_logits, torch.float32, "pen_logits", (R, V))
+    acc = ctypes.c_int32(0)
+    ne = ctypes.c_int32(0)
+    pol = policy.c()
+    _check(lib().vr_verify_window_host(_ptr(weight), _host_ptr(act_h, torch.float32, "act_h"), R, H,
+                                       V, path, _host_ptr(tokens_h, torch.int32, "tokens_h"),
+                                       _host_ptr(parent_h, torch.int32, "parent_h"), n,
+                                       _host_ptr(q_ids_h, torch.int32, "q_ids_h"),
+                                       _host_ptr(q_logits_h, torch.float32, "q_logits_h"),
+                                       _host_ptr(hist_h, torch.int32, "hist_h"),
+                                       0 if hist_h is None else hist_h.numel(), ctypes.byref(pol),
+                                       seed, position, _ptr(logits), _ptr(pen_logits),
+                                       _host_ptr(out_ids_h, torch.int32, "out_ids_h"),
+                                       ctypes.byref(acc), ctypes.byref(ne), _ptr(ws), ws.numel(),
+                                       _stream(stream, logits.device)), "vr_verify_window_host")
+    return acc.value, ne.value

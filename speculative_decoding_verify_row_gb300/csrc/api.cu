@@ -1,0 +1,423 @@
+// C ABI of libverifyrow: argument validation, workspace layout and the
+// order of launches of each entry point.  See include/verifyrow.h.
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "vr_common.cuh"
+#include "vr_kernels.h"
+
+namespace vr {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Layout {
+  size_t status, planes, cand, pool_ids, pool_vals, pol_e, pol_m, pol_S, q_pen, reqs, row_req;
+  size_t st_act, st_tok, st_par, st_qid, st_qlog, st_hist, st_out, total;
+};
+
+Layout layout(int rows, int hidden, int vocab) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kAlign);
+    return at;
+  };
+  const size_t r = static_cast<size_t>(rows);
+  L.status = take(kAlign);
+  L.planes = take(tc_plane_bytes(rows, hidden));
+  L.cand = take(select_cand_bytes(rows, vocab));
+  L.pool_ids = take(r * kPool * 4);
+  L.pool_vals = take(r * kPool * 4);
+  L.pol_e = take(r * kPool * 8);
+  L.pol_m = take(r * 4);
+  L.pol_S = take(r * 8);
+  L.q_pen = take(r * kQCand * 4);
+  L.reqs = take(std::min<size_t>(r, VR_MAX_REQUESTS) * sizeof(ReqDev));
+  L.row_req = take(r * 4);
+  L.st_act = take(r * hidden * 4);
+  L.st_tok = take(r * 4);
+  L.st_par = take(r * 4);
+  L.st_qid = take(r * kQCand * 4);
+  L.st_qlog = take(r * kQCand * 4);
+  L.st_hist = take(VR_MAX_PENALTY_WINDOW * 4);
+  L.st_out = take((r + 2) * 4);
+  L.total = off;
+  return L;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+int check_policy(const vr_policy* p) {
+  if (!p) return VR_ERR_ARG;
+  if (!finite(p->temperature) || p->temperature < 0.f) return VR_ERR_ARG;
+  if (!finite(p->min_p) || !finite(p->top_p)) return VR_ERR_ARG;
+  if (!finite(p->repeat) || p->repeat <= 0.f) return VR_ERR_ARG;
+  if (!finite(p->presence) || !finite(p->frequency)) return VR_ERR_ARG;
+  if (p->window < 0 || p->window > VR_MAX_PENALTY_WINDOW) return VR_ERR_ARG;
+  return VR_OK;
+}
+
+bool active(const vr_policy& p) {
+  return p.window > 0 && (p.repeat != 1.f || p.presence != 0.f || p.frequency != 0.f);
+}
+
+int check_shape(int rows, int hidden, int vocab) {
+  if (rows < 1 || rows > VR_MAX_ROWS) return VR_ERR_ARG;
+  if (vocab < 1) return VR_ERR_ARG;
+  if (hidden < 8 || hidden > 65536) return VR_ERR_ARG;
+  if (hidden % 8) return VR_ERR_UNSUPPORTED;
+  return VR_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, int rows, int hidden, int vocab) {
+  if (!ws || reinterpret_cast<uintptr_t>(ws) % kAlign) return VR_ERR_WORKSPACE;
+  if (ws_bytes < layout(rows, hidden, vocab).total) return VR_ERR_WORKSPACE;
+  return VR_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_window(int rows, int n_nodes, const int32_t* tokens, const int32_t* q_ids,
+                 const float* q_logits, const int32_t* hist, int hist_len) {
+  if (n_nodes < 0 || rows != n_nodes + 1 || rows > VR_MAX_WINDOW_ROWS) return VR_ERR_ARG;
+  if (n_nodes > 0 && !tokens) return VR_ERR_ARG;
+  if ((q_ids == nullptr) != (q_logits == nullptr)) return VR_ERR_ARG;
+  if (hist_len < 0 || (hist_len > 0 && !hist)) return VR_ERR_ARG;
+  return VR_OK;
+}
+
+ReqDev make_req(int row0, int n_nodes, const int32_t* tokens, const int32_t* parent,
+                const int32_t* q_ids, const float* q_in, float* q_pen, const int32_t* hist,
+                int hist_len, const vr_policy& pol, uint64_t seed, uint64_t position,
+                int32_t* out_ids, int32_t* out_accept, int32_t* out_n) {
+  ReqDev r{};
+  r.row0 = row0;
+  r.n_nodes = n_nodes;
+  r.tokens = tokens;
+  r.parent = parent;
+  r.q_ids = q_ids;
+  r.q_logits_in = q_in;
+  r.q_pen = q_pen;
+  r.hist = hist;
+  r.hist_len = hist_len;
+  r.pol = pol;
+  r.seed = seed;
+  r.position = position;
+  r.out_ids = out_ids;
+  r.out_accept = out_accept;
+  r.out_n = out_n;
+  return r;
+}
+
+ReqTable single(const ReqDev& r) {
+  ReqTable t{};
+  t.one = r;
+  t.many = nullptr;
+  t.row_req = nullptr;
+  t.n_req = 1;
+  return t;
+}
+
+
+int project(const uint16_t* weight, const float* act, int rows, int hidden, int vocab, int path,
+            float* logits, void* ws, const Layout& L, cudaStream_t s) {
+  if (path == VR_PATH_AUTO) path = VR_PATH_TC;
+  if (path == VR_PATH_TC)
+    return launch_project_tc(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
+                             at<int32_t>(ws, L.status), s);
+  if (path == VR_PATH_FFMA) return launch_project_ffma(weight, act, rows, hidden, vocab, logits, s);
+  return VR_ERR_ARG;
+}
+
+// penalties -> pool + policy -> acceptance, for requests already in `tab`
+int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* target,
+                  bool any_active, bool any_q, void* ws, const Layout& L, cudaStream_t s) {
+  int st;
+  if (any_active) {
+    st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);
+    if (st != VR_OK) return st;
+  }
+  st = launch_select(target, rows, vocab, at<uint64_t>(ws, L.cand), at<int32_t>(ws, L.pool_ids),
+                     at<float>(ws, L.pool_vals), &tab, at<double>(ws, L.pol_e),
+                     at<int32_t>(ws, L.pol_m), at<double>(ws, L.pol_S), s);
+  if (st != VR_OK) return st;
+  return launch_accept(tab, n_req, vocab, at<int32_t>(ws, L.pool_ids), at<double>(ws, L.pol_e),
+                       at<int32_t>(ws, L.pol_m), at<double>(ws, L.pol_S),
+                       at<float>(ws, L.q_pen), at<int32_t>(ws, L.status), s);
+}
+
+int window_device(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
+                  int path, const int32_t* tokens, const int32_t* parent, int n_nodes,
+                  const int32_t* q_ids, const float* q_logits, const int32_t* hist, int hist_len,
+                  const vr_policy& pol, uint64_t seed, uint64_t position, float* logits,
+                  float* pen_logits, int32_t* out_ids, int32_t* out_accept, int32_t* out_n,
+                  void* ws, const Layout& L, cudaStream_t s) {
+  int st = project(weight, act, rows, hidden, vocab, path, logits, ws, L, s);
+  if (st != VR_OK) return st;
+  const bool act_pen = active(pol);
+  float* target = logits;
+  if (act_pen && pen_logits) {
+    if (cudaMemcpyAsync(pen_logits, logits, static_cast<size_t>(rows) * vocab * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return VR_ERR_CUDA;
+    target = pen_logits;
+  }
+  float* q_pen = (act_pen && q_ids) ? at<float>(ws, L.q_pen) : const_cast<float*>(q_logits);
+  const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_pen, hist,
+                                       hist_len, pol, seed, position, out_ids, out_accept, out_n));
+  return sample_stages(tab, 1, rows, vocab, target, act_pen, q_ids != nullptr, ws, L, s);
+}
+
+}  // namespace
+}  // namespace vr
+
+using namespace vr;
+
+extern "C" {
+
+int vr_abi_version(void) { return VR_ABI_VERSION; }
+
+const char* vr_status_string(int status) {
+  switch (status) {
+    case VR_OK: return "ok";
+    case VR_ERR_ARG: return "invalid argument";
+    case VR_ERR_CUDA: return "CUDA error";
+    case VR_ERR_UNSUPPORTED: return "unsupported shape";
+    case VR_ERR_DEVICE: return "device status word set";
+    case VR_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int vr_workspace_bytes(int rows, int hidden, int vocab, size_t* out_bytes) {
+  if (!out_bytes) return VR_ERR_ARG;
+  const int st = check_shape(rows, hidden, vocab);
+  if (st != VR_OK) return st;
+  *out_bytes = layout(rows, hidden, vocab).total;
+  return VR_OK;
+}
+
+int vr_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kAlign || reinterpret_cast<uintptr_t>(ws) % kAlign) return VR_ERR_WORKSPACE;
+  return cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
+int vr_verify_project(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
+                      int path, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_shape(rows, hidden, vocab);
+  if (st != VR_OK) return st;
+  if (!weight || !act || !logits) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC) return VR_ERR_ARG;
+  if (!aligned16(weight)) return VR_ERR_ARG;
+  if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
+  return project(weight, act, rows, hidden, vocab, path, logits, ws, layout(rows, hidden, vocab),
+                 static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_penalize(float* logits, int rows, int vocab, const int32_t* tokens,
+                       const int32_t* parent, int n_nodes, const int32_t* hist, int hist_len,
+                       const vr_policy* policy, const int32_t* q_ids, float* q_logits, void* ws,
+                       size_t ws_bytes, void* stream) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if (!logits || vocab < 1) return VR_ERR_ARG;
+  if ((st = check_window(rows, n_nodes, tokens, q_ids, q_logits, hist, hist_len)) != VR_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
+  if (!active(*policy)) return VR_OK;
+  const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_logits, hist,
+                                       hist_len, *policy, 0, 0, nullptr, nullptr, nullptr));
+  const Layout L = layout(rows, 8, vocab);
+  return launch_penalize(tab, rows, logits, vocab, q_ids != nullptr, at<int32_t>(ws, L.status),
+                         static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids,
+                     float* pool_vals, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_shape(rows, 8, vocab);
+  if (st != VR_OK) return st;
+  if (!logits || !pool_ids || !pool_vals) return VR_ERR_ARG;
+  if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, 8, vocab);
+  return launch_select(logits, rows, vocab, at<uint64_t>(ws, L.cand), pool_ids, pool_vals,
+                       nullptr, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,
+                     int32_t* out_m, double* out_e, double* out_S, void* stream) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if (!pool_vals || !out_m || !out_e || !out_S) return VR_ERR_ARG;
+  if (rows < 1 || rows > VR_MAX_ROWS || pool_len < 1 || pool_len > VR_POOL) return VR_ERR_ARG;
+  return launch_policy(pool_vals, rows, pool_len, *policy, out_m, out_e, out_S,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab, const int32_t* tokens,
+                            const int32_t* parent, int n_nodes, const int32_t* q_ids,
+                            const float* q_logits, const vr_policy* policy, uint64_t seed,
+                            uint64_t position, int32_t* out_ids, int32_t* out_accept,
+                            int32_t* out_n_emitted, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if (!pen_logits || vocab < 1 || !out_ids || !out_accept || !out_n_emitted) return VR_ERR_ARG;
+  if ((st = check_window(rows, n_nodes, tokens, q_ids, q_logits, nullptr, 0)) != VR_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, 8, vocab);
+  const ReqTable tab =
+      single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, const_cast<float*>(q_logits),
+                      nullptr, 0, *policy, seed, position, out_ids, out_accept, out_n_emitted));
+  return sample_stages(tab, 1, rows, vocab, const_cast<float*>(pen_logits), false, false, ws, L,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_window(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
+                     int path, const int32_t* tokens, const int32_t* parent, int n_nodes,
+                     const int32_t* q_ids, const float* q_logits, const int32_t* hist,
+                     int hist_len, const vr_policy* policy, uint64_t seed, uint64_t position,
+                     float* logits, float* pen_logits, int32_t* out_ids, int32_t* out_accept,
+                     int32_t* out_n_emitted, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
+  if (!weight || !act || !logits || !out_ids || !out_accept || !out_n_emitted) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC || !aligned16(weight)) return VR_ERR_ARG;
+  if ((st = check_window(rows, n_nodes, tokens, q_ids, q_logits, hist, hist_len)) != VR_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
+  return window_device(weight, act, rows, hidden, vocab, path, tokens, parent, n_nodes, q_ids,
+                       q_logits, hist, hist_len, *policy, seed, position, logits, pen_logits,
+                       out_ids, out_accept, out_n_emitted, ws, layout(rows, hidden, vocab),
+                       static_cast<cudaStream_t>(stream));
+}
+
+int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidden, int vocab,
+                             int path, const vr_request* reqs, int n_req, float* logits,
+                             float* pen_logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!reqs || n_req < 1 || n_req > VR_MAX_REQUESTS) return VR_ERR_ARG;
+  if (!weight || !act || !logits || !aligned16(weight)) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC) return VR_ERR_ARG;
+  int rows = 0, st;
+  bool any_active = false, any_q = false;
+  for (int b = 0; b < n_req; ++b) {
+    const vr_request& r = reqs[b];
+    if ((st = check_policy(&r.policy)) != VR_OK) return st;
+    if ((st = check_window(r.n_nodes + 1, r.n_nodes, r.tokens, r.q_ids, r.q_logits, r.hist,
+                           r.hist_len)) != VR_OK)
+      return st;
+    if (!r.out_ids || !r.out_accept || !r.out_n_emitted) return VR_ERR_ARG;
+    rows += r.n_nodes + 1;
+    if (rows > VR_MAX_ROWS) return VR_ERR_ARG;
+    any_active |= active(r.policy);
+    any_q |= r.q_ids != nullptr;
+  }
+  if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, hidden, vocab);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  std::vector<ReqDev> table(n_req);
+  std::vector<int32_t> row_req(rows);
+  int row0 = 0;
+  for (int b = 0; b < n_req; ++b) {
+    const vr_request& r = reqs[b];
+    float* q_pen = (active(r.policy) && r.q_ids) ? at<float>(ws, L.q_pen) + static_cast<size_t>(row0) * kQCand
+                                                : const_cast<float*>(r.q_logits);
+    table[b] = make_req(row0, r.n_nodes, r.tokens, r.parent, r.q_ids, r.q_logits, q_pen, r.hist,
+                        r.hist_len, r.policy, r.seed, r.position, r.out_ids, r.out_accept,
+                        r.out_n_emitted);
+    for (int i = 0; i <= r.n_nodes; ++i) row_req[row0 + i] = b;
+    row0 += r.n_nodes + 1;
+  }
+  if (cudaMemcpyAsync(at<void>(ws, L.reqs), table.data(), table.size() * sizeof(ReqDev),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(at<void>(ws, L.row_req), row_req.data(), row_req.size() * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return VR_ERR_CUDA;
+
+  st = project(weight, act, rows, hidden, vocab, path, logits, ws, L, s);
+  if (st != VR_OK) return st;
+  float* target = logits;
+  if (any_active && pen_logits) {
+    if (cudaMemcpyAsync(pen_logits, logits, static_cast<size_t>(rows) * vocab * sizeof(float),
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return VR_ERR_CUDA;
+    target = pen_logits;
+  }
+  ReqTable tab{};
+  tab.many = at<ReqDev>(ws, L.reqs);
+  tab.row_req = at<int32_t>(ws, L.row_req);
+  tab.n_req = n_req;
+  return sample_stages(tab, n_req, rows, vocab, target, any_active, any_q, ws, L, s);
+}
+
+int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
+                          int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,
+                          int n_nodes, const int32_t* q_ids_h, const float* q_logits_h,
+                          const int32_t* hist_h, int hist_len, const vr_policy* policy,
+                          uint64_t seed, uint64_t position, float* logits, float* pen_logits,
+                          int32_t* out_ids_h, int32_t* out_accept_h, int32_t* out_n_emitted_h,
+                          void* ws, size_t ws_bytes, void* stream) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
+  if (!weight || !act_h || !logits || !out_ids_h || !out_accept_h || !out_n_emitted_h)
+    return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC || !aligned16(weight)) return VR_ERR_ARG;
+  if ((st = check_window(rows, n_nodes, tokens_h, q_ids_h, q_logits_h, hist_h, hist_len)) != VR_OK)
+    return st;
+  if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, hidden, vocab);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int h_keep = std::min(hist_len, VR_MAX_PENALTY_WINDOW);
+  auto h2d = [&](size_t off, const void* src, size_t bytes) {
+    return bytes == 0 || cudaMemcpyAsync(at<void>(ws, off), src, bytes, cudaMemcpyHostToDevice, s) ==
+                             cudaSuccess;
+  };
+  if (!h2d(L.st_act, act_h, static_cast<size_t>(rows) * hidden * 4) ||
+      !h2d(L.st_tok, tokens_h, static_cast<size_t>(n_nodes) * 4) ||
+      (parent_h && !h2d(L.st_par, parent_h, static_cast<size_t>(n_nodes) * 4)) ||
+      (q_ids_h && !h2d(L.st_qid, q_ids_h, static_cast<size_t>(n_nodes) * kQCand * 4)) ||
+      (q_logits_h && !h2d(L.st_qlog, q_logits_h, static_cast<size_t>(n_nodes) * kQCand * 4)) ||
+      (h_keep > 0 && !h2d(L.st_hist, hist_h + (hist_len - h_keep), static_cast<size_t>(h_keep) * 4)))
+    return VR_ERR_CUDA;
+  int32_t* out = at<int32_t>(ws, L.st_out);
+  st = window_device(weight, at<float>(ws, L.st_act), rows, hidden, vocab, path,
+                     at<int32_t>(ws, L.st_tok), parent_h ? at<int32_t>(ws, L.st_par) : nullptr,
+                     n_nodes, q_ids_h ? at<int32_t>(ws, L.st_qid) : nullptr,
+                     q_logits_h ? at<float>(ws, L.st_qlog) : nullptr, at<int32_t>(ws, L.st_hist),
+                     h_keep, *policy, seed, position, logits, pen_logits, out + 2, out, out + 1,
+                     ws, L, s);
+  if (st != VR_OK) return st;
+  int32_t head[2];
+  if (cudaMemcpyAsync(head, out, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_ids_h, out + 2, static_cast<size_t>(rows) * sizeof(int32_t),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return VR_ERR_CUDA;
+  *out_accept_h = head[0];
+  *out_n_emitted_h = head[1];
+  return VR_OK;
+}
+
+int vr_device_status(void* ws, int32_t* out_status, void* stream) {
+  if (!ws || !out_status) return VR_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return VR_ERR_CUDA;
+  *out_status = v;
+  return VR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+"""GPU pool select and sampler policy, bit for bit against the oracle
+("Speculative decoding on RDNA" §03: fixed pool, tie order and summation)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as ov
+from speculative_decoding_verify_row_gb300 import binding as vb
+from gpu_common import require_gpu, dev, same_bits_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def adversarial_rows(R, V, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((R, V)).astype(np.float32)
+    kind = seed % 4
+    if kind == 1:                       # heavy ties from a small value set
+        x = rng.choice(np.float32([2.5, 1.0, 0.0, -0.0, -1.0]), size=(R, V)).astype(np.float32)
+    elif kind == 2:                     # specials sprinkled in
+        specials = np.float32([np.inf, -np.inf, np.nan, 0.0, -0.0, 3.0e38, -3.0e38, 1e-45])
+        mask = rng.random((R, V)) < 0.2
+        x[mask] = rng.choice(specials, size=mask.sum())
+        neg_nan = rng.random((R, V)) < 0.01
+        x[neg_nan] = np.frombuffer(np.uint32(0xFFC00123).tobytes(), np.float32)[0]
+    elif kind == 3:                     # all equal: pure id order
+        x[:] = np.float32(0.5)
+    return x
+
+
+def gpu_pool(x):
+    R, V = x.shape
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    ws = vb.workspace(R, 8, V)
+    vb.verify_select(dev(x), ids, vals, ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), vals.cpu().numpy()
+
+
+@pytest.mark.parametrize("V", [1, 7, 63, 64, 65, 2047, 2048, 2049, 5000, 151936, 400000])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3])
+def test_pool_matches_oracle(V, kind):
+    R = 3 if V > 100000 else 5
+    x = adversarial_rows(R, V, 100 * V + kind)
+    ids, vals = gpu_pool(x)
+    n = min(64, V)
+    for r in range(R):
+        ref_ids, ref_vals = ov.target_pool(x[r])
+        assert np.array_equal(ids[r, :n], ref_ids), (r, ids[r, :n], ref_ids)
+        assert np.array_equal(vals[r, :n].view(np.uint32), ref_vals.view(np.uint32))
+        assert np.all(ids[r, n:] == -1)
+
+
+def test_pool_of_the_tree_rows():
+    x = adversarial_rows(25, 151936, 8)
+    ids, _ = gpu_pool(x)
+    for r in range(25):
+        assert np.array_equal(ids[r], ov.target_pool(x[r])[0])
+
+
+POLICIES = [
+    ov.Policy(temperature=0.0),
+    ov.Policy(temperature=0.7),
+    ov.Policy(temperature=0.7, top_k=0, min_p=0.05, top_p=0.95),
+    ov.Policy(temperature=1.0, top_k=5),
+    ov.Policy(temperature=3.0, top_k=0),
+    ov.Policy(temperature=0.05, top_k=0, top_p=0.5),
+    ov.Policy(temperature=1.3, top_k=100, min_p=0.3),
+    ov.Policy(temperature=0.8, top_k=1),
+    ov.Policy(temperature=1e-30, top_k=0),
+    ov.Policy(temperature=2.0, top_k=0, top_p=0.0),
+    ov.Policy(temperature=0.9, top_k=0, min_p=2.0),
+]
+
+
+def pools_for_policy(seed):
+    rng = np.random.default_rng(seed)
+    v = -np.sort(-(rng.standard_normal((12, 64)) * rng.uniform(0.1, 8, (12, 1)))).astype(np.float32)
+    v[3, 40:] = -np.inf
+    v[4, 10:] = np.nan
+    v[5, :] = v[5, 0]
+    v[6, 20:] = v[6, 19]
+    v[7, 1:] = -np.float32(3e38)
+    return v
+
+
+@pytest.mark.parametrize("pi", range(len(POLICIES)))
+@pytest.mark.parametrize("pool_len", [64, 8, 3, 1])
+def test_policy_bit_exact(pi, pool_len):
+    pol = POLICIES[pi]
+    v = pools_for_policy(pi * 10 + pool_len)
+    R = v.shape[0]
+    m = torch.empty(R, dtype=torch.int32, device="cuda")
+    e = torch.empty((R, 64), dtype=torch.float64, device="cuda")
+    S = torch.empty(R, dtype=torch.float64, device="cuda")
+    vb.verify_policy(dev(v), pool_len, vb.Policy(**pol.__dict__), m, e, S)
+    torch.cuda.synchronize()
+    m, e, S = m.cpu().numpy(), e.cpu().numpy(), S.cpu().numpy()
+    for r in range(R):
+        rm, re, rS = ov.policy_weights(v[r, :pool_len], pol)
+        assert m[r] == rm
+        assert np.array_equal(e[r, :rm].view(np.uint64), np.array(re, np.float64).view(np.uint64))
+        assert np.all(e[r, rm:] == 0.0)
+        assert np.float64(S[r]).view(np.uint64) == np.float64(rS).view(np.uint64)

@@ -1,0 +1,324 @@
+"""The fused window on the GPU against the oracle, on the workloads of the
+benchmark suite: tiny greedy chain, sampled chain (k 3), penalised chain
+(k 8), token tree (3 x 8), batched serving (64 requests), plus the
+multi-window history rule and the host-buffer entry point.
+
+Parity here is stage-wise, so that no oracle input comes from the CUDA path:
+  * logits: GPU vs the fp64 oracle, |d| <= 1e-3 * max(1, |ref|);
+  * sampling: GPU sample_accept and the oracle on the same float32 logits
+    (float32 of the oracle's fp64 logits): penalised rows, pools, ids and
+    accept counts bit for bit;
+  * the fused window's ids equal the GPU's own sample_accept on the window's
+    logits, and equal the oracle's ids whenever both sides' pools agree (a
+    near-tie in float32 can legitimately reorder a pool; such a window is
+    counted, not compared)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as ov
+from speculative_decoding_verify_row_gb300 import binding as vb, synth
+from gpu_common import require_gpu, dev, dev_weight, assert_logits_close, same_bits_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def bpol(p):
+    return vb.Policy(**p.__dict__)
+
+
+def run_window(wd, act, tokens, pol, seed, position, parent=None, q_ids=None, q_log=None,
+               hist=None, path=vb.VR_PATH_AUTO, separate_pen=True):
+    R, H = act.shape
+    V = wd.shape[0]
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(logits) if separate_pen else None
+    out = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ne = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = vb.workspace(R, H, V)
+    vb.verify_window(wd, dev(act), dev(tokens) if len(tokens) else None, bpol(pol), seed, position,
+                     logits, out, acc, ne, ws, parent=None if parent is None else dev(parent),
+                     q_ids=None if q_ids is None else dev(q_ids),
+                     q_logits=None if q_log is None else dev(q_log),
+                     hist=None if hist is None or len(hist) == 0 else dev(hist), pen_logits=pen,
+                     path=path)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    penalised = pen if (pen is not None and ov.penalties_active(pol)) else logits
+    return dict(logits=logits, pen=penalised, ids=out.cpu().numpy(), accept=int(acc.item()),
+                n=int(ne.item()))
+
+
+def gpu_sample(pen_np, tokens, pol, seed, position, parent=None, q_ids=None, q_pen=None):
+    R, V = pen_np.shape
+    out = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ne = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = vb.workspace(R, 8, V)
+    vb.verify_sample_accept(dev(pen_np), dev(tokens) if len(tokens) else None, bpol(pol), seed,
+                            position, out, acc, ne, ws, parent=None if parent is None else dev(parent),
+                            q_ids=None if q_ids is None else dev(q_ids),
+                            q_logits=None if q_pen is None else dev(q_pen))
+    torch.cuda.synchronize()
+    return list(out.cpu().numpy()[:int(ne.item())]), int(acc.item())
+
+
+def check_window(win, ref_logits64, tokens, pol, seed, position, parent=None, q_ids=None,
+                 q_log=None, hist=(), stats=None, logit_cols=None):
+    """All stage-wise checks of one fused GPU window (see module doc)."""
+    g_logits = win["logits"]
+    if logit_cols is None:
+        assert_logits_close(g_logits.cpu().numpy(), ref_logits64)
+    else:
+        c = torch.from_numpy(logit_cols).cuda()
+        assert_logits_close(g_logits[:, c].cpu().numpy(), ref_logits64[:, logit_cols])
+    plist = ov.chain_parents(len(tokens)) if parent is None else [int(p) for p in parent]
+    ref32 = ref_logits64.astype(np.float32)
+    # (1) oracle and GPU sampler on the same float32 logits
+    ref = ov.verify_window(ref32, tokens, plist, q_ids, q_log, hist, pol, seed, position)
+    g_ids, g_acc = gpu_sample(ref.pen_logits, tokens, pol, seed, position, parent, q_ids, ref.q_pen)
+    assert (g_ids, g_acc) == (ref.emitted, ref.accept)
+    # (2) the fused window equals the GPU's own stages run one by one on its
+    # raw logits (penalize, then sample_accept)
+    R, V = g_logits.shape
+    pen_again = g_logits.clone()
+    q_again = None if q_log is None else dev(q_log)
+    ws = vb.workspace(R, 8, V)
+    vb.verify_penalize(pen_again, dev(tokens) if len(tokens) else None,
+                       dev(np.asarray(hist, np.int32)) if len(hist) else None, bpol(pol), ws,
+                       parent=None if parent is None else dev(parent),
+                       q_ids=None if q_ids is None else dev(q_ids), q_logits=q_again)
+    torch.cuda.synchronize()
+    assert torch.equal(pen_again.view(torch.int32), win["pen"].view(torch.int32))
+    g_pen = win["pen"].cpu().numpy()
+    own_ids, own_acc = gpu_sample(g_pen, tokens, pol, seed, position, parent, q_ids,
+                                  None if q_again is None else q_again.cpu().numpy())
+    assert list(win["ids"][:win["n"]]) == own_ids and win["accept"] == own_acc
+    assert 1 <= win["n"] == win["accept"] + 1
+    # (3) end to end against the oracle when both sides' pools agree
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    vb.verify_select(win["pen"].contiguous(), ids, vals, ws)
+    torch.cuda.synchronize()
+    ids = ids.cpu().numpy()
+    same_pools = all(np.array_equal(ids[r, :len(ref.pool_ids[r])], ref.pool_ids[r]) for r in range(R))
+    if stats is not None:
+        stats["windows"] = stats.get("windows", 0) + 1
+        stats["compared"] = stats.get("compared", 0) + int(same_pools)
+    if same_pools:
+        assert list(win["ids"][:win["n"]]) == ref.emitted and win["accept"] == ref.accept
+    return ref
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_FFMA])
+def test_tiny_greedy_chain(path):
+    """hidden 256, vocab 4096, k 3; drafts = the oracle's argmax chain with
+    row 2 perturbed: two drafts accepted, three tokens emitted."""
+    W = synth.weights(4096, 256)
+    A = synth.activations(4, 256, 0)
+    L64 = ov.project(W, A)
+    am = [int(ov.target_pool(L64[r].astype(np.float32))[0][0]) for r in range(4)]
+    drafts = synth.perturb_draft(am, 3, 2, 4096, seed=0)
+    win = run_window(dev_weight(W), A, drafts, ov.Policy(), 0, 100, path=path)
+    ref = check_window(win, L64, drafts, ov.Policy(), 0, 100)
+    assert ref.accept == 2 and win["accept"] == 2 and win["n"] == 3
+    assert list(win["ids"][:3]) == am[:2] + [am[2]]
+
+
+def chain_inputs(bw, k, window_seed, pol_q_temp=0.7):
+    A = synth.activations(k + 1, bw.hidden, window_seed)
+    L64 = bw.oracle_logits(A)
+    top = [ov.target_pool(L64[r].astype(np.float32)) for r in range(k + 1)]
+    t32_ids = np.stack([t[0][:32] for t in top[:k]])
+    t32_val = np.stack([t[1][:32] for t in top[:k]])
+    q_ids, q_log = synth.draft_candidates(t32_ids, t32_val, seed=window_seed)
+    slot = synth.draft_choice(q_log, pol_q_temp, seed=window_seed + 1)
+    drafts = q_ids[np.arange(k), slot].astype(np.int32)
+    return A, L64, q_ids, q_log, drafts
+
+
+def cols_sample(V, seed, n=2000):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.integers(0, V, n), [0, V - 1]]))
+
+
+def test_sampled_chain_full_size(big_weights_4096):
+    """hidden 4096, vocab 151936, k 3; T 0.7, top-k absent, min-p 0.05,
+    top-p 0.95, no penalties; several window seeds."""
+    bw = big_weights_4096
+    pol = ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95)
+    stats = {}
+    for s in range(6):
+        A, L64, q_ids, q_log, drafts = chain_inputs(bw, 3, s)
+        win = run_window(bw.dev, A, drafts, pol, s, 4096 + s, q_ids=q_ids, q_log=q_log)
+        check_window(win, L64, drafts, pol, s, 4096 + s, q_ids=q_ids, q_log=q_log, stats=stats)
+    assert stats["compared"] >= 4
+
+
+def test_penalised_chain_full_size(big_weights_4096):
+    """k 8 (9 rows), 4096-token Zipf(1.1) history, W 64, repeat 1.1,
+    presence 1.5, frequency 0.2, top-k 0 (the 64-wide pool).  The last
+    window plants row 0's pool tokens in the last 64 history slots, so that
+    the penalties reorder the pool."""
+    bw = big_weights_4096
+    pol = ov.Policy(temperature=0.7, top_k=0, min_p=0.05, top_p=0.95, repeat=1.1, presence=1.5,
+                    frequency=0.2, window=64)
+    stats = {}
+    for s in range(3):
+        A, L64, q_ids, q_log, drafts = chain_inputs(bw, 8, 100 + s)
+        hist = synth.zipf_history(4096, 151936, seed=100 + s)
+        if s == 2:
+            hist[-64:] = ov.target_pool(L64[0].astype(np.float32))[0][:64]
+        for separate in (True, False):
+            win = run_window(bw.dev, A, drafts, pol, s, 4096, q_ids=q_ids, q_log=q_log, hist=hist,
+                             separate_pen=separate)
+            ref = check_window(win, L64, drafts, pol, s, 4096, q_ids=q_ids, q_log=q_log, hist=hist,
+                               stats=stats, logit_cols=cols_sample(151936, s) if separate else None)
+        if s == 2:
+            raw_pool = ov.target_pool(L64[0].astype(np.float32))[0]
+            assert not np.array_equal(ref.pool_ids[0], raw_pool)
+    assert stats["compared"] >= 4
+
+
+@pytest.mark.parametrize("temperature", [0.0, 0.7])
+def test_token_tree_full_size(big_weights_4096, temperature):
+    """3 branches x depth 8 (24 nodes, 25 rows); branch 0 agrees with the
+    target for 5 nodes.  Greedy: longest agreeing branch; sampled (T 0.7,
+    top-k 20): naive descent with per-node penalty histories (W 64,
+    presence 1.5)."""
+    bw = big_weights_4096
+    parent = synth.tree_parents(3, 8)
+    pol = ov.Policy(temperature=temperature, top_k=20, presence=1.5, window=64)
+    stats = {}
+    for s in range(3):
+        A = synth.activations(25, 4096, 200 + s)
+        L64 = bw.oracle_logits(A)
+        pools = [ov.target_pool(L64[r].astype(np.float32))[0] for r in range(25)]
+        tokens = synth.tree_tokens([p[0] for p in pools], [p[:32] for p in pools], seed=200 + s)
+        hist = synth.zipf_history(2048, 151936, seed=200 + s)
+        win = run_window(bw.dev, A, tokens, pol, s, 2048, parent=parent, hist=hist)
+        ref = check_window(win, L64, tokens, pol, s, 2048, parent=parent, hist=hist, stats=stats,
+                           logit_cols=cols_sample(151936, 300 + s))
+        if temperature == 0.0:
+            assert ref.accept >= 5          # branch 0 agrees for 5 nodes at least
+    assert stats["compared"] >= 2
+
+
+def test_batched_serving(big_weights_5120):
+    """64 requests x k 3 (256 rows), hidden 5120; even requests greedy, odd
+    ones T 0.8 / top-k 20 / top-p 0.9 / presence 1.5; 2048-token Zipf
+    histories, W 64, seeds 0..63.  Checked on 8 requests against the
+    oracle, on all of them against the GPU's own per-request windows."""
+    bw = big_weights_5120
+    nreq, k, H, V = 64, 3, 5120, 151936
+    A = synth.activations(nreq * (k + 1), H, 500)
+    check = set(range(0, nreq, 8)) | {1, 63}
+    rows = [r for b in sorted(check) for r in range(b * (k + 1), (b + 1) * (k + 1))]
+    L64_rows = bw.oracle_logits(A[rows])
+    L64 = {b: L64_rows[i * (k + 1):(i + 1) * (k + 1)] for i, b in enumerate(sorted(check))}
+    reqs, keep, specs = [], [], []
+    rng = np.random.default_rng(500)
+    for b in range(nreq):
+        greedy = b % 2 == 0
+        pol = ov.Policy() if greedy else ov.Policy(temperature=0.8, top_k=20, top_p=0.9,
+                                                   presence=1.5, window=64)
+        hist = synth.zipf_history(2048, V, seed=1000 + b)
+        # draft candidates around a plausible region (the top-32 is known
+        # only for the checked requests; the rest use random ids)
+        if b in L64:
+            top = [ov.target_pool(L64[b][r].astype(np.float32)) for r in range(k)]
+            q_ids, q_log = synth.draft_candidates(np.stack([t[0][:32] for t in top]),
+                                                  np.stack([t[1][:32] for t in top]), seed=b)
+        else:
+            q_ids = rng.integers(0, V, (k, 8)).astype(np.int32)
+            q_log = rng.standard_normal((k, 8)).astype(np.float32)
+        slot = synth.draft_choice(q_log, 0.0 if greedy else 0.8, seed=b + 7)
+        drafts = q_ids[np.arange(k), slot].astype(np.int32)
+        t = dict(tok=dev(drafts), q=dev(q_ids), ql=dev(q_log), h=dev(hist),
+                 out=torch.full((k + 1,), -7, dtype=torch.int32, device="cuda"),
+                 acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                 n=torch.zeros(1, dtype=torch.int32, device="cuda"))
+        keep.append(t)
+        specs.append((drafts, q_ids, q_log, hist, pol))
+        reqs.append(vb.make_request(k, t["tok"], bpol(pol), b, 2048, t["out"], t["acc"], t["n"],
+                                    q_ids=t["q"], q_logits=t["ql"], hist=t["h"]))
+    R = nreq * (k + 1)
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(logits)
+    ws = vb.workspace(R, H, V)
+    vb.verify_window_batched(bw.dev, dev(A), reqs, logits, ws, pen_logits=pen)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    stats = {}
+    for b in range(nreq):
+        drafts, q_ids, q_log, hist, pol = specs[b]
+        sl = slice(b * (k + 1), (b + 1) * (k + 1))
+        penalised = pen if ov.penalties_active(pol) else logits
+        win = dict(logits=logits[sl], pen=penalised[sl], ids=keep[b]["out"].cpu().numpy(),
+                   accept=int(keep[b]["acc"].item()), n=int(keep[b]["n"].item()))
+        if b in L64:
+            check_window(win, L64[b], drafts, pol, b, 2048, q_ids=q_ids, q_log=q_log, hist=hist,
+                         stats=stats, logit_cols=cols_sample(V, b, 500))
+        else:
+            scratch = win["logits"].clone()
+            q_pen = dev(q_log)
+            vb.verify_penalize(scratch, dev(drafts), dev(hist), bpol(pol), vb.workspace(k + 1, 8, V),
+                               q_ids=dev(q_ids), q_logits=q_pen)
+            torch.cuda.synchronize()
+            own_ids, own_acc = gpu_sample(win["pen"].cpu().numpy(), drafts, pol, b, 2048, None,
+                                          q_ids, q_pen.cpu().numpy())
+            assert list(win["ids"][:win["n"]]) == own_ids and win["accept"] == own_acc
+    assert stats["compared"] >= 6
+
+
+def test_multi_window_history():
+    """Four consecutive windows of one request: the next history is the old
+    one plus the emitted ids only (never a rejected draft), and the
+    position advances by the number emitted."""
+    rng = np.random.default_rng(9)
+    V, H, k = 5000, 256, 4
+    W = synth.weights(V, H)
+    wd = dev_weight(W)
+    pol = ov.Policy(temperature=0.9, top_k=0, presence=1.5, frequency=0.3, window=16)
+    hist = list(rng.integers(0, V, 40))
+    position = len(hist)
+    for w in range(4):
+        A = synth.activations(k + 1, H, 700 + w)
+        L64 = ov.project(W, A)
+        top = [ov.target_pool(L64[r].astype(np.float32)) for r in range(k)]
+        q_ids, q_log = synth.draft_candidates(np.stack([t[0][:32] for t in top]),
+                                              np.stack([t[1][:32] for t in top]), seed=w)
+        drafts = q_ids[np.arange(k), synth.draft_choice(q_log, 0.9, seed=w)].astype(np.int32)
+        win = run_window(wd, A, drafts, pol, 42, position, q_ids=q_ids, q_log=q_log,
+                         hist=np.array(hist, np.int32))
+        ref = check_window(win, L64, drafts, pol, 42, position, q_ids=q_ids, q_log=q_log, hist=hist)
+        emitted = [int(t) for t in win["ids"][:win["n"]]]
+        rejected = [int(d) for d in drafts[win["accept"]:]]
+        hist = hist + emitted
+        position += len(emitted)
+        assert hist[-len(emitted):] == emitted
+        if rejected and win["accept"] < k:
+            assert hist[len(hist) - len(emitted):] == emitted
+
+
+def test_host_entry_point_matches_device_entry_point(big_weights_4096):
+    bw = big_weights_4096
+    pol = ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95, presence=1.5, window=64)
+    A, L64, q_ids, q_log, drafts = chain_inputs(bw, 3, 77)
+    hist = synth.zipf_history(4096, 151936, seed=77)
+    win = run_window(bw.dev, A, drafts, pol, 77, 4096, q_ids=q_ids, q_log=q_log, hist=hist)
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    logits = torch.empty((4, 151936), dtype=torch.float32, device="cuda")
+    out = pin(np.full(4, -7, np.int32))
+    ws = vb.workspace(4, 4096, 151936)
+    acc, n = vb.verify_window_host(bw.dev, pin(A), pin(drafts), bpol(pol), 77, 4096, logits, out, ws,
+                                   q_ids_h=pin(q_ids), q_logits_h=pin(q_log), hist_h=pin(hist))
+    assert (acc, n) == (win["accept"], win["n"])
+    assert list(out.numpy()[:n]) == list(win["ids"][:n])
+    assert torch.equal(logits, win["logits"])
