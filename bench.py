@@ -46,6 +46,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mode", choices=["full", "window", "project"], default="full",
+                   help="window: only the timed windows (for a profiler's launch list); "
+                        "project: only the projection of one window (for a kernel capture)")
     return p.parse_args()
 
 
@@ -214,6 +217,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_projection_only(torch, vb, synth, wd, dev, args):
+    """The projection of one 4-row window, warm-up + steps times."""
+    a = torch.from_numpy(synth.activations(ROWS, H, 0)).to(dev)
+    lg = torch.empty((ROWS, V), dtype=torch.float32, device=dev)
+    ws = vb.workspace(ROWS, H, V, device=dev)
+    for _ in range(args.warmup):
+        vb.verify_project(wd, a, lg, ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vb.verify_project(wd, a, lg, ws)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"mode": "project", "steps": args.steps,
+                      "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -231,6 +250,9 @@ def main():
 
     W = synth.weights(V, H)
     wd = torch.from_numpy(W.view(np.int16)).to(dev)
+    if args.mode == "project":
+        run_projection_only(torch, vb, synth, wd, dev, args)
+        return
     win = make_windows(torch, vb, synth, wd, dev)
     pol = vb.Policy(**POLICY)
     logits = torch.empty((ROWS, V), dtype=torch.float32, device=dev)
@@ -270,6 +292,13 @@ def main():
     if vb.device_status(ws) != 0:
         raise RuntimeError("device status set during the timed region")
 
+    if args.mode == "window":
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "windows/s", "mode": "window",
+                              "steps": args.steps, "warmup": args.warmup}), flush=True)
+        replicas.shutdown()
+        return
+
     # ---- stage breakdown: the same windows through the stage entry points,
     # events between stages on the launching stream ----
     n_stage = min(args.steps, 2000)
@@ -288,6 +317,16 @@ def main():
     proj_ms = [e[0].elapsed_time(e[1]) for e in evs]
     samp_ms = [e[1].elapsed_time(e[2]) for e in evs]
     proj_avg_s = statistics.fmean(proj_ms) / 1000.0
+    # the pool select alone, on the same logits
+    pool_vals = torch.empty((ROWS, 64), dtype=torch.float32, device=dev)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(200):
+        vb.verify_select(logits, pool_ids, pool_vals, ws, stream=stream)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    select_us = 1000.0 * s0.elapsed_time(s1) / 200
 
     # ---- window cost against rows (projection stage, both paths) ----
     sweep = {}
@@ -351,6 +390,7 @@ def main():
                      "algorithmic_bytes_per_launch": WEIGHT_BYTES},
         "stages_us": {"projection": 1000.0 * statistics.fmean(proj_ms),
                       "pool_policy_accept": 1000.0 * statistics.fmean(samp_ms),
+                      "pool_select_only": select_us,
                       "window": 1e6 * job_s / args.steps},
         "rows_sweep_us": sweep,
         "clocks": clocks.summary(),

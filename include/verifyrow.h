@@ -177,18 +177,20 @@ VR_API int vr_verify_select(const float* logits, int rows, int vocab, int32_t* p
 /*
  * (a4) Sampler policy on given pools ("Speculative decoding on RDNA" §03):
  * pool_vals [rows][64] in pool order, pool_len valid entries per row.
- * K = 20 if top_k absent, 64 if 0, else min(top_k, 64), at most pool_len;
- * greedy (temperature 0) keeps pool[0] alone with weight 1; otherwise
- * e_0 = 1, e_j = vexp((v_j - v_0) / T) in double (0 for NaN or -inf), then
- * min-p cuts at the first e_j < min_p, top-p keeps the shortest prefix
- * whose running sum reaches top_p * sum, and S is the sequential sum.
- * vexp is a Cody-Waite reduction plus a degree-13 Taylor polynomial in IEEE
- * double +, -, x only, so results are identical on every IEEE machine.
+ * All arithmetic is IEEE float32, each operation rounded to nearest, sums
+ * sequential in pool order.  K = 20 if top_k absent, 64 if 0, else
+ * min(top_k, 64), at most pool_len; greedy (temperature 0) keeps pool[0]
+ * alone with weight 1; otherwise e_0 = 1, e_j = vexp((v_j - v_0) / T)
+ * (0 for NaN or -inf, or an exponent below -87), then min-p cuts at the
+ * first e_j < min_p, top-p keeps the shortest prefix whose running sum
+ * reaches top_p * sum, and S is the sum of the kept weights.  vexp is a
+ * Cody-Waite reduction plus a degree-7 Taylor polynomial in float32 +, -, x
+ * only, so results are identical on every IEEE machine.
  * Outputs: out_m [rows] kept count, out_e [rows][64] (zeros past m),
  * out_S [rows].
  */
 VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,
-                     int32_t* out_m, double* out_e, double* out_S, void* stream);
+                     int32_t* out_m, float* out_e, float* out_S, void* stream);
 
 /*
  * (a3)+(a4)+(a5) Pool, policy and acceptance on already-penalised logits.
@@ -206,8 +208,9 @@ VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, cons
  *     the root draw y ~ p(row); move to the lowest-index child carrying y,
  *     else emit y and stop.
  * Draws: u = Philox4x64-10(counter = (position, row, purpose, 0),
- * key = (seed, 0)) word 0 >> 11, times 2^-53; purpose 1 = accept uniform,
- * 2 = emitted draw; t = u * S picks the first j whose running sum exceeds t.
+ * key = (seed, 0)) word 0 >> 40, times 2^-24 (a float32); purpose 1 = accept
+ * uniform, 2 = emitted draw; t = u * S picks the first j whose running sum
+ * exceeds t.  The probabilities, accept test and residual are float32.
  * Outputs: out_ids [n_nodes + 1] (emitted ids, then untouched), out_accept,
  * out_n_emitted (= accepted + 1 >= 1; 0 if the device status was set).
  */

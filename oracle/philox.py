@@ -17,7 +17,10 @@ where it is used:
 
     key     = (seed, 0)
     counter = (position, row, purpose, 0)
-    u       = (first output word >> 11) * 2**-53      in [0, 1)
+    u       = (first output word >> 40) * 2**-24      in [0, 1), a float32
+
+(24 random bits, exactly representable in float32, the precision in which
+the policy decides draws and accept tests).
 
 purpose 0 = a draft draw (used by the tests to draw drafts from q),
 purpose 1 = the accept uniform of a row, purpose 2 = the emit draw of a row
@@ -56,9 +59,9 @@ def philox4x64_10(counter, key):
 
 
 def uniform(seed, position, row, purpose):
-    """The uniform in [0, 1) that the window draws at (row, purpose)."""
+    """The float32 uniform in [0, 1) that the window draws at (row, purpose)."""
     w0 = philox4x64_10((position, row, purpose, 0), (seed, 0))[0]
-    return (w0 >> 11) * 2.0 ** -53
+    return np.float32(w0 >> 40) * np.float32(2.0 ** -24)
 
 
 # ---------------------------------------------------------------------------
@@ -109,4 +112,4 @@ def uniform_array(seeds, position, row, purpose):
     z = np.zeros_like(seeds)
     w0 = philox4x64_10_array(z + np.uint64(position), z + np.uint64(row),
                              z + np.uint64(purpose), z, seeds, z)[0]
-    return (w0 >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    return (w0 >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)

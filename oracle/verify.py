@@ -238,23 +238,28 @@ def candidate_pool(cand_ids, cand_vals):
 # (a4) policy -- "Speculative decoding on RDNA" §03 ("how hipfire does it"):
 # temperature, top-k (absent = 20, 0 = the 64-wide pool), min-p and top-p,
 # with the same pool, tie order and summation as the AR sampler.  Reading of
-# the order and arithmetic (all f64, sums sequential in pool order):
+# the order and arithmetic (the pages fix neither): every step is one
+# float32 operation rounded to nearest, sums run sequentially in pool order,
 #   K = 20 if top_k absent, 64 if 0, else min(top_k, 64); K <= pool size
 #   T == 0: greedy, p = point mass on pool[0]
 #   e_0 = 1; e_j = vexp((v_j - v_0) / T) for j < K (0 if v_j is NaN or -inf,
-#        or the exponent is below -708 or NaN)
+#        or the exponent is below -87 or NaN)
 #   min-p: cut the prefix at the first j >= 1 with e_j < min_p (e_j/e_0 is
 #          p_j/p_max, so this keeps p_j >= min_p * p_max)
 #   top-p: with S the sum of the survivors, keep the shortest prefix whose
 #          running sum reaches top_p * S
 #   S = sum of the kept e; p_j = e_j / S
 
+F32 = np.float32
+
+
 @dataclass
 class RowDist:
-    """A policy applied to one pool: the kept ids and unnormalised weights."""
+    """A policy applied to one pool: the kept ids and unnormalised weights
+    (float32)."""
     ids: list
     e: list
-    total: float
+    total: np.float32
 
     @property
     def m(self):
@@ -270,45 +275,46 @@ def topk_limit(top_k):
 
 
 def seq_sum(xs):
-    s = 0.0
+    s = F32(0.0)
     for x in xs:
-        s += x
+        s = F32(s + F32(x))
     return s
 
 
 def policy_weights(pool_vals, pol):
-    """(m, e[:m], S) for one pool (values in pool order)."""
+    """(m, e[:m], S) for one pool (values in pool order), all float32."""
     n = len(pool_vals)
     if n == 0:
         raise ValueError("empty pool")
     K = min(topk_limit(pol.top_k), n)
     if pol.greedy:
-        return 1, [1.0], 1.0
-    T = float(pol.temperature)
-    v0 = float(pool_vals[0])
-    e = [1.0]
-    for j in range(1, K):
-        v = float(pool_vals[j])
-        if math.isnan(v) or v == -math.inf:
-            e.append(0.0)
-            continue
-        z = (v - v0) / T
-        e.append(vexp(z) if z >= Z_MIN else 0.0)
-    m = K
-    if pol.min_p > 0.0:
-        mp = float(pol.min_p)
-        j = 1
-        while j < m and e[j] >= mp:
-            j += 1
-        m = j
-    if pol.top_p < 1.0:
-        thr = float(pol.top_p) * seq_sum(e[:m])
-        c = 0.0
-        for j in range(m):
-            c += e[j]
-            if c >= thr:
-                m = j + 1
-                break
+        return 1, [F32(1.0)], F32(1.0)
+    T = F32(pol.temperature)
+    v0 = F32(pool_vals[0])
+    e = [F32(1.0)]
+    with np.errstate(all="ignore"):
+        for j in range(1, K):
+            v = F32(pool_vals[j])
+            if np.isnan(v) or v == -np.inf:
+                e.append(F32(0.0))
+                continue
+            z = F32(F32(v - v0) / T)
+            e.append(vexp(z) if z >= Z_MIN else F32(0.0))
+        m = K
+        if pol.min_p > 0.0:
+            mp = F32(pol.min_p)
+            j = 1
+            while j < m and e[j] >= mp:
+                j += 1
+            m = j
+        if pol.top_p < 1.0:
+            thr = F32(F32(pol.top_p) * seq_sum(e[:m]))
+            c = F32(0.0)
+            for j in range(m):
+                c = F32(c + e[j])
+                if c >= thr:
+                    m = j + 1
+                    break
     e = e[:m]
     return m, e, seq_sum(e)
 
@@ -320,10 +326,10 @@ def row_dist(pool_ids, pool_vals, pol):
 
 def prob_of(dist, x):
     """p(x) = e_j / S for the kept entry holding x (summed over repeats)."""
-    acc = 0.0
+    acc = F32(0.0)
     for t, ej in zip(dist.ids, dist.e):
         if t == x:
-            acc += ej / dist.total
+            acc = F32(acc + F32(ej / dist.total))
     return acc
 
 
@@ -333,10 +339,10 @@ def prob_of(dist, x):
 # entry with a positive weight.
 
 def draw_index(weights, total, u):
-    t = u * total
-    c = 0.0
+    t = F32(F32(u) * F32(total))
+    c = F32(0.0)
     for j, w in enumerate(weights):
-        c += w
+        c = F32(c + F32(w))
         if c > t:
             return j
     for j in range(len(weights) - 1, -1, -1):
@@ -386,8 +392,8 @@ def accept_rejection_chain(pdists, qdists, drafts, uniforms, replacement="residu
         x = int(x)
         p, q = pdists[i], qdists[i]
         px, qx = prob_of(p, x), prob_of(q, x)
-        u1 = uniforms(i, PURPOSE_ACCEPT)
-        accepted = (u1 * qx < px) if qx > 0.0 else (px > 0.0)
+        u1 = F32(uniforms(i, PURPOSE_ACCEPT))
+        accepted = (F32(u1 * qx) < px) if qx > 0.0 else (px > 0.0)
         if accepted:
             emitted.append(x)
             continue
@@ -398,8 +404,8 @@ def accept_rejection_chain(pdists, qdists, drafts, uniforms, replacement="residu
             return emitted, i
         resid = []
         for t, ej in zip(p.ids, p.e):
-            d = ej / p.total - prob_of(q, t)
-            resid.append(d if d > 0.0 else 0.0)
+            d = F32(F32(ej / p.total) - prob_of(q, t))
+            resid.append(d if d > 0.0 else F32(0.0))
         sr = seq_sum(resid)
         j = draw_index(resid, sr, u2) if sr > 0.0 else draw_index(p.e, p.total, u2)
         emitted.append(p.ids[j])

@@ -226,8 +226,8 @@ def verify_policy(pool_vals, pool_len, policy, out_m, out_e, out_S, stream=None)
     R = pool_vals.shape[0]
     _dev(pool_vals, torch.float32, "pool_vals", (R, VR_POOL))
     _dev(out_m, torch.int32, "out_m", (R,))
-    _dev(out_e, torch.float64, "out_e", (R, VR_POOL))
-    _dev(out_S, torch.float64, "out_S", (R,))
+    _dev(out_e, torch.float32, "out_e", (R, VR_POOL))
+    _dev(out_S, torch.float32, "out_S", (R,))
     pol = policy.c()
     _check(lib().vr_verify_policy(_ptr(pool_vals), R, pool_len, ctypes.byref(pol), _ptr(out_m),
                                   _ptr(out_e), _ptr(out_S), _stream(stream, pool_vals.device)),

@@ -13,7 +13,7 @@ namespace {
 constexpr size_t kAlign = 256;
 
 struct Layout {
-  size_t status, planes, cand, pool_ids, pool_vals, pol_e, pol_m, pol_S, q_pen, reqs, row_req;
+  size_t status, planes, cand, pool_ids, pool_vals, dec, q_pen, reqs, row_req;
   size_t st_act, st_tok, st_par, st_qid, st_qlog, st_hist, st_out, total;
 };
 
@@ -31,9 +31,7 @@ Layout layout(int rows, int hidden, int vocab) {
   L.cand = take(select_cand_bytes(rows, vocab));
   L.pool_ids = take(r * kPool * 4);
   L.pool_vals = take(r * kPool * 4);
-  L.pol_e = take(r * kPool * 8);
-  L.pol_m = take(r * 4);
-  L.pol_S = take(r * 8);
+  L.dec = take(r * sizeof(int4));
   L.q_pen = take(r * kQCand * 4);
   L.reqs = take(std::min<size_t>(r, VR_MAX_REQUESTS) * sizeof(ReqDev));
   L.row_req = take(r * 4);
@@ -146,12 +144,9 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
     if (st != VR_OK) return st;
   }
   st = launch_select(target, rows, vocab, at<uint64_t>(ws, L.cand), at<int32_t>(ws, L.pool_ids),
-                     at<float>(ws, L.pool_vals), &tab, at<double>(ws, L.pol_e),
-                     at<int32_t>(ws, L.pol_m), at<double>(ws, L.pol_S), s);
+                     at<float>(ws, L.pool_vals), &tab, at<int4>(ws, L.dec), s);
   if (st != VR_OK) return st;
-  return launch_accept(tab, n_req, vocab, at<int32_t>(ws, L.pool_ids), at<double>(ws, L.pol_e),
-                       at<int32_t>(ws, L.pol_m), at<double>(ws, L.pol_S),
-                       at<float>(ws, L.q_pen), at<int32_t>(ws, L.status), s);
+  return launch_accept(tab, n_req, vocab, at<int4>(ws, L.dec), at<int32_t>(ws, L.status), s);
 }
 
 int window_device(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
@@ -249,11 +244,11 @@ int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids
   if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
   const Layout L = layout(rows, 8, vocab);
   return launch_select(logits, rows, vocab, at<uint64_t>(ws, L.cand), pool_ids, pool_vals,
-                       nullptr, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                       nullptr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,
-                     int32_t* out_m, double* out_e, double* out_S, void* stream) {
+                     int32_t* out_m, float* out_e, float* out_S, void* stream) {
   int st = check_policy(policy);
   if (st != VR_OK) return st;
   if (!pool_vals || !out_m || !out_e || !out_S) return VR_ERR_ARG;

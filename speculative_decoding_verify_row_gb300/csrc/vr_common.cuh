@@ -3,7 +3,9 @@
 // Every floating-point step that decides an integer (a pool order, a kept
 // count, a draw) uses explicit round-to-nearest intrinsics, so that no
 // fused multiply-add or fast-math rewrite can change a bit; the library is
-// also compiled with --fmad=false.
+// also compiled with --fmad=false.  The sampler works in float32 (the pages
+// fix no precision; GB300's double-precision latency made the per-row
+// decisions a tenth of the window).
 #pragma once
 
 #include <cstdint>
@@ -86,7 +88,7 @@ __device__ __forceinline__ uint32_t packed_id(uint64_t p) {
 
 // ---------------------------------------------------------------------------
 // Philox4x64-10 (Salmon et al., SC'11): counter (position, row, purpose, 0),
-// key (seed, 0); u = (word0 >> 11) * 2^-53.
+// key (seed, 0); u = (word0 >> 40) * 2^-24, a float32 in [0, 1).
 
 constexpr uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ull;
 constexpr uint64_t kPhiloxM1 = 0xCA5A826395121157ull;
@@ -115,42 +117,37 @@ __device__ __forceinline__ uint64_t philox_word0(uint64_t c0, uint64_t c1, uint6
   return c0;
 }
 
-__device__ __forceinline__ double uniform01(uint64_t seed, uint64_t position, uint64_t row,
-                                            uint64_t purpose) {
+__device__ __forceinline__ float uniform01(uint64_t seed, uint64_t position, uint64_t row,
+                                           uint64_t purpose) {
   const uint64_t w = philox_word0(position, row, purpose, 0ull, seed, 0ull);
-  return __dmul_rn(__ull2double_rn(w >> 11), 0x1p-53);
+  return __fmul_rn(__uint2float_rn(static_cast<uint32_t>(w >> 40)), 0x1p-24f);
 }
 
 // ---------------------------------------------------------------------------
-// vexp: Cody-Waite reduction by ln 2 (C1 = ln 2 with its low 32 significand
-// bits cleared, C2 = nearest double to ln 2 - C1), degree-13 Taylor
-// polynomial of e^r in Horner form (coefficients 1/j! rounded to nearest),
-// scaling by 2^n from the exponent bits.  IEEE double +, -, x only.
+// vexp: Cody-Waite reduction by ln 2 (C1 = ln 2 in float32 with its low 8
+// significand bits cleared, C2 = nearest float32 to ln 2 - C1), degree-7
+// Taylor polynomial of e^r in Horner form (coefficients: the float32 nearest
+// to 1/j!), scaling by 2^n from the exponent bits.  float32 +, -, x only,
+// each rounded to nearest; 0 below -87, so every result is normal.
 
-__device__ __forceinline__ double vexp(double z) {
-  if (!(z >= -708.0)) return 0.0;
-  if (z > 709.0) return __longlong_as_double(0x7FF0000000000000ll);
-  constexpr double kInvLn2 = 0x1.71547652b82fep+0;
-  constexpr double kC1 = 0x1.62e4200000000p-1;
-  constexpr double kC2 = 0x1.fdf473de6af28p-22;
-  const double nf = rint(__dmul_rn(z, kInvLn2));
-  const double r = __dsub_rn(__dsub_rn(z, __dmul_rn(nf, kC1)), __dmul_rn(nf, kC2));
-  double p = 0x1.6124613a86d09p-33;                    // 1/13!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.1eed8eff8d898p-29);  // 1/12!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.ae64567f544e4p-26);  // 1/11!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.27e4fb7789f5cp-22);  // 1/10!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.71de3a556c734p-19);  // 1/9!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.a01a01a01a01ap-16);  // 1/8!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.a01a01a01a01ap-13);  // 1/7!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.6c16c16c16c17p-10);  // 1/6!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.1111111111111p-7);   // 1/5!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.5555555555555p-5);   // 1/4!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.5555555555555p-3);   // 1/3!
-  p = __dadd_rn(__dmul_rn(p, r), 0x1.0000000000000p-1);   // 1/2!
-  p = __dadd_rn(__dmul_rn(p, r), 1.0);                    // 1/1!
-  p = __dadd_rn(__dmul_rn(p, r), 1.0);                    // 1/0!
-  const long long n = static_cast<long long>(nf);
-  return __dmul_rn(p, __longlong_as_double((n + 1023ll) << 52));
+__device__ __forceinline__ float vexp(float z) {
+  if (!(z >= -87.0f)) return 0.0f;
+  if (z > 88.0f) return __int_as_float(0x7f800000);
+  const float kInvLn2 = __int_as_float(0x3fb8aa3b);
+  const float kC1 = __int_as_float(0x3f317200);
+  const float kC2 = __int_as_float(0x35bfbe8e);
+  const float nf = rintf(__fmul_rn(z, kInvLn2));
+  const float r = __fsub_rn(__fsub_rn(z, __fmul_rn(nf, kC1)), __fmul_rn(nf, kC2));
+  float p = __int_as_float(0x39500d01);                       // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), __int_as_float(0x3ab60b61));  // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), __int_as_float(0x3c088889));  // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), __int_as_float(0x3d2aaaab));  // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), __int_as_float(0x3e2aaaab));  // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);                        // 1/2!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                        // 1/1!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                        // 1/0!
+  const int n = static_cast<int>(nf);
+  return __fmul_rn(p, __int_as_float((n + 127) << 23));
 }
 
 // ---------------------------------------------------------------------------
@@ -176,31 +173,31 @@ __device__ __forceinline__ int topk_limit(int32_t top_k) {
 }
 
 __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_policy& pol,
-                                            double* e, int* m_out, double* S_out) {
+                                            float* e, int* m_out, float* S_out) {
   const int lane = threadIdx.x & 31;
   int K = topk_limit(pol.top_k);
   if (K > n) K = n;
   if (pol.temperature == 0.f) {
-    for (int j = lane; j < kPool; j += 32) e[j] = (j == 0) ? 1.0 : 0.0;
+    for (int j = lane; j < kPool; j += 32) e[j] = (j == 0) ? 1.0f : 0.0f;
     __syncwarp();
     if (lane == 0) {
       *m_out = 1;
-      *S_out = 1.0;
+      *S_out = 1.0f;
     }
     __syncwarp();
     return;
   }
-  const double T = static_cast<double>(pol.temperature);
-  const double v0 = static_cast<double>(vals[0]);
+  const float T = pol.temperature;
+  const float v0 = vals[0];
   for (int j = lane; j < kPool; j += 32) {
-    double ej = 0.0;
+    float ej = 0.0f;
     if (j == 0) {
-      ej = 1.0;
+      ej = 1.0f;
     } else if (j < K) {
       const float v = vals[j];
       if (!(isnan(v) || v == -__int_as_float(0x7f800000))) {
-        const double z = __ddiv_rn(__dsub_rn(static_cast<double>(v), v0), T);
-        ej = (z >= -708.0) ? vexp(z) : 0.0;
+        const float z = __fdiv_rn(__fsub_rn(v, v0), T);
+        ej = (z >= -87.0f) ? vexp(z) : 0.0f;
       }
     }
     e[j] = ej;
@@ -209,54 +206,30 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
   if (lane == 0) {
     int m = K;
     if (pol.min_p > 0.f) {
-      const double mp = static_cast<double>(pol.min_p);
       int j = 1;
-      while (j < m && e[j] >= mp) ++j;
+      while (j < m && e[j] >= pol.min_p) ++j;
       m = j;
     }
     if (pol.top_p < 1.f) {
-      double s = 0.0;
-      for (int j = 0; j < m; ++j) s = __dadd_rn(s, e[j]);
-      const double thr = __dmul_rn(static_cast<double>(pol.top_p), s);
-      double c = 0.0;
+      float s = 0.0f;
+      for (int j = 0; j < m; ++j) s = __fadd_rn(s, e[j]);
+      const float thr = __fmul_rn(pol.top_p, s);
+      float c = 0.0f;
       for (int j = 0; j < m; ++j) {
-        c = __dadd_rn(c, e[j]);
+        c = __fadd_rn(c, e[j]);
         if (c >= thr) {
           m = j + 1;
           break;
         }
       }
     }
-    double S = 0.0;
-    for (int j = 0; j < m; ++j) S = __dadd_rn(S, e[j]);
-    for (int j = m; j < kPool; ++j) e[j] = 0.0;
+    float S = 0.0f;
+    for (int j = 0; j < m; ++j) S = __fadd_rn(S, e[j]);
+    for (int j = m; j < kPool; ++j) e[j] = 0.0f;
     *m_out = m;
     *S_out = S;
   }
   __syncwarp();
-}
-
-// t = u * S; the first j whose running sum exceeds t; if rounding leaves
-// none, the last j with a positive weight.
-__device__ __forceinline__ int draw_index(const double* w, int n, double total, double u) {
-  const double t = __dmul_rn(u, total);
-  double c = 0.0;
-  for (int j = 0; j < n; ++j) {
-    c = __dadd_rn(c, w[j]);
-    if (c > t) return j;
-  }
-  for (int j = n - 1; j >= 0; --j)
-    if (w[j] > 0.0) return j;
-  return 0;
-}
-
-// p(x) = sum over kept entries holding x of e_j / S, in pool order.
-__device__ __forceinline__ double prob_of(const int32_t* ids, const double* e, int m, double S,
-                                          int32_t x) {
-  double acc = 0.0;
-  for (int j = 0; j < m; ++j)
-    if (ids[j] == x) acc = __dadd_rn(acc, __ddiv_rn(e[j], S));
-  return acc;
 }
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) {

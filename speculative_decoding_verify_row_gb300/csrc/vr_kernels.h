@@ -21,20 +21,19 @@ int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int 
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab,
                     bool with_q, int32_t* status, cudaStream_t stream);
 
-// pool select (+ optional policy): logits [rows][vocab] ->
-// pool ids/vals [rows][64], and if tab != nullptr e/m/S per row
+// pool select: logits [rows][vocab] -> pool ids/vals [rows][64]; with a
+// request table also the policy and the per-row decisions
+// dec[row] = (argmax, emit draw y, residual draw z, accept bit)
 int select_segments(int vocab);
 size_t select_cand_bytes(int rows, int vocab);
 int launch_select(const float* logits, int rows, int vocab, uint64_t* cand, int32_t* pool_ids,
-                  float* pool_vals, const ReqTable* tab, double* pol_e, int32_t* pol_m,
-                  double* pol_S, cudaStream_t stream);
+                  float* pool_vals, const ReqTable* tab, int4* dec, cudaStream_t stream);
 
 int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
-                  int32_t* out_m, double* out_e, double* out_S, cudaStream_t stream);
+                  int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream);
 
 // acceptance: one CTA per request
-int launch_accept(const ReqTable& tab, int n_req, int vocab, const int32_t* pool_ids,
-                  const double* pol_e, const int32_t* pol_m, const double* pol_S,
-                  const float* q_pen, int32_t* status, cudaStream_t stream);
+int launch_accept(const ReqTable& tab, int n_req, int vocab, const int4* dec, int32_t* status,
+                  cudaStream_t stream);
 
 }  // namespace vr

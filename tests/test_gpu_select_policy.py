@@ -97,14 +97,14 @@ def test_policy_bit_exact(pi, pool_len):
     v = pools_for_policy(pi * 10 + pool_len)
     R = v.shape[0]
     m = torch.empty(R, dtype=torch.int32, device="cuda")
-    e = torch.empty((R, 64), dtype=torch.float64, device="cuda")
-    S = torch.empty(R, dtype=torch.float64, device="cuda")
+    e = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    S = torch.empty(R, dtype=torch.float32, device="cuda")
     vb.verify_policy(dev(v), pool_len, vb.Policy(**pol.__dict__), m, e, S)
     torch.cuda.synchronize()
     m, e, S = m.cpu().numpy(), e.cpu().numpy(), S.cpu().numpy()
     for r in range(R):
         rm, re, rS = ov.policy_weights(v[r, :pool_len], pol)
         assert m[r] == rm
-        assert np.array_equal(e[r, :rm].view(np.uint64), np.array(re, np.float64).view(np.uint64))
+        assert np.array_equal(e[r, :rm].view(np.uint32), np.array(re, np.float32).view(np.uint32))
         assert np.all(e[r, rm:] == 0.0)
-        assert np.float64(S[r]).view(np.uint64) == np.float64(rS).view(np.uint64)
+        assert np.float32(S[r]).view(np.uint32) == np.float32(rS).view(np.uint32)

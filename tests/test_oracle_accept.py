@@ -85,7 +85,8 @@ def test_single_branch_tree_is_the_chain_rule():
 
 
 def _dist(ids, probs):
-    return ov.RowDist(list(ids), list(probs), float(np.sum(probs)))
+    probs = [np.float32(x) for x in probs]
+    return ov.RowDist(list(ids), probs, ov.seq_sum(probs))
 
 
 def test_accept_predicate_is_min_one_p_over_q():
@@ -192,11 +193,12 @@ def test_rejection_sampling_is_exact_by_enumeration(V, k, T, seed):
             for d, t in enumerate(em):
                 reach[d] += pd * w
                 at_depth[d, t] += pd * w
-    assert abs(first.sum() - 1.0) < 1e-12
-    np.testing.assert_allclose(first, p_ref[0], atol=1e-12)
+    # exact up to the float32 rounding of the policy (a few 1e-7)
+    assert abs(first.sum() - 1.0) < 1e-9
+    np.testing.assert_allclose(first, p_ref[0], atol=2e-6)
     for d in range(1, k + 1):
-        if reach[d] > 1e-6:
-            np.testing.assert_allclose(at_depth[d] / reach[d], p_ref[d], atol=1e-10)
+        if reach[d] > 1e-3:
+            np.testing.assert_allclose(at_depth[d] / reach[d], p_ref[d], atol=2e-5)
 
 
 def test_naive_descent_is_exact_for_a_deterministic_tree():
@@ -222,9 +224,9 @@ def test_naive_descent_is_exact_for_a_deterministic_tree():
         first[em[0]] += w
         if em[0] == 0 and len(em) > 1:
             second_after_0[em[1]] += w
-    np.testing.assert_allclose(first, p_ref[0], atol=1e-12)
+    np.testing.assert_allclose(first, p_ref[0], atol=2e-6)
     # token 0 at the root is node 0 (the lowest index); its row is 1
-    np.testing.assert_allclose(second_after_0 / second_after_0.sum(), p_ref[1], atol=1e-12)
+    np.testing.assert_allclose(second_after_0 / second_after_0.sum(), p_ref[1], atol=2e-5)
 
 
 def test_every_window_emits_at_least_one_token():

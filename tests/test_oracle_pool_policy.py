@@ -53,11 +53,12 @@ def test_greedy_and_topk_one_are_argmax():
     assert ov.policy_weights(vals, ov.Policy(temperature=0.0)) == (1, [1.0], 1.0)
     m, e, S = ov.policy_weights(vals, ov.Policy(temperature=1.0, top_k=1))
     assert (m, e, S) == (1, [1.0], 1.0)
+    assert isinstance(S, np.float32) and isinstance(e[0], np.float32)
 
 
 def _probs(vals, pol):
     m, e, S = ov.policy_weights(np.float32(vals), pol)
-    return np.array([x / S for x in e])
+    return np.array([float(x) / float(S) for x in e])
 
 
 def test_full_pool_is_softmax():
@@ -66,7 +67,8 @@ def test_full_pool_is_softmax():
         vals = np.sort(rng.standard_normal(64).astype(np.float32) * 3)[::-1]
         p = _probs(vals, ov.Policy(temperature=T, top_k=0))
         ref = softmax(vals.astype(np.float64) / np.float64(np.float32(T)))
-        np.testing.assert_allclose(p, ref, rtol=1e-13, atol=1e-300)
+        # float32 policy: each weight within a few float32 ulps of the softmax
+        np.testing.assert_allclose(p, ref, rtol=1e-5, atol=1e-30)   # z itself is rounded to float32
 
 
 def test_topk_absent_is_twenty():
@@ -85,7 +87,7 @@ def test_min_p_keeps_tokens_above_fraction_of_max():
         ref = softmax(vals.astype(np.float64) / np.float64(np.float32(T)))
         ratio = ref / ref[0]
         mp32 = float(np.float32(mp))
-        if np.min(np.abs(ratio - mp32)) < 1e-9:
+        if np.min(np.abs(ratio - mp32)) < 1e-5:
             continue
         p = _probs(vals, ov.Policy(temperature=T, top_k=0, min_p=mp))
         assert len(p) == int(np.sum(ratio >= mp32))
@@ -99,17 +101,17 @@ def test_top_p_keeps_the_smallest_prefix_reaching_the_mass():
         ref = softmax(vals.astype(np.float64) / np.float64(np.float32(T)))
         cum = np.cumsum(ref)
         tp32 = float(np.float32(tp))
-        if np.min(np.abs(cum - tp32)) < 1e-9:
+        if np.min(np.abs(cum - tp32)) < 1e-5:
             continue
         p = _probs(vals, ov.Policy(temperature=T, top_k=0, top_p=tp))
         assert len(p) == int(np.argmax(cum >= tp32)) + 1
-        np.testing.assert_allclose(p, ref[:len(p)] / ref[:len(p)].sum(), rtol=1e-12)
+        np.testing.assert_allclose(p, ref[:len(p)] / ref[:len(p)].sum(), rtol=1e-5)
 
 
 def test_low_temperature_tends_to_argmax():
     vals = np.float32([2.0, 1.9, 1.0])
     p = _probs(vals, ov.Policy(temperature=0.001, top_k=0))
-    assert p[0] == 1.0 and 0.0 < p[1] < 1e-40
+    assert p[0] == 1.0 and p[1] == 0.0          # e_1 = exp(-100) is below the float32 range
 
 
 def test_nan_and_minus_inf_get_no_mass():
@@ -120,11 +122,11 @@ def test_nan_and_minus_inf_get_no_mass():
 
 def test_draw_matches_weights():
     """The draw rule maps u-intervals to entries with lengths e_j / S."""
-    e = [1.0, 0.5, 0.0, 0.25, 0.125]
+    e = [np.float32(x) for x in (1.0, 0.5, 0.0, 0.25, 0.125)]
     S = ov.seq_sum(e)
     N = 100_000
     counts = np.zeros(len(e))
     for i in range(N):
         counts[ov.draw_index(e, S, (i + 0.5) / N)] += 1
-    np.testing.assert_allclose(counts / N, np.array(e) / S, atol=2.0 / N)
-    assert ov.draw_index(e, S, 1.0 - 2**-53) == 4
+    np.testing.assert_allclose(counts / N, np.array(e, np.float64) / float(S), atol=2.0 / N)
+    assert ov.draw_index(e, S, np.float32(1.0 - 2**-24)) == 4

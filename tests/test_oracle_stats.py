@@ -66,7 +66,7 @@ def _simulate(name, replacement):
 def _chi2_p(samples, dist):
     probs = {}
     for t, e in zip(dist.ids, dist.e):
-        probs[t] = probs.get(t, 0.0) + e / dist.total
+        probs[t] = probs.get(t, 0.0) + float(e) / float(dist.total)
     ids = sorted(probs, key=lambda t: -probs[t])
     n = len(samples)
     if np.any(~np.isin(samples, ids)):
