@@ -175,6 +175,28 @@ VR_API int vr_verify_select(const float* logits, int rows, int vocab, int32_t* p
                      float* pool_vals, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * vr_verify_select without a workspace.  The pages have no counterpart: this
+ * entry point exists for callers that cannot give the library device memory
+ * of its own (for example a plugin whose host application owns every device
+ * allocation, or a process that must not grow its device footprint after
+ * start-up).  Same inputs, outputs and results as vr_verify_select; the
+ * select's intermediate candidates live in a fixed 1.25 MiB array compiled
+ * into the library, which every GPU that loads the library keeps until exit.
+ * Limits and rules:
+ *   - rows <= VR_NOALLOC_SELECT_MAX_ROWS (else VR_ERR_UNSUPPORTED); any vocab;
+ *   - the array is shared by all calls on a device and keeps the last call's
+ *     contents; calls that overlap on the GPU race on it, so the caller must
+ *     serialise them (one stream, one thread at a time);
+ *   - the first call on each device looks the array's address up on that
+ *     device (cudaGetSymbolAddress, the device must be current); make that
+ *     first call before any stream capture on the device.
+ * Allocates nothing (no cudaMalloc or cudaFree, on any call).
+ */
+#define VR_NOALLOC_SELECT_MAX_ROWS 32
+VR_API int vr_verify_select_noalloc(const float* logits, int rows, int vocab, int32_t* pool_ids,
+                                    float* pool_vals, void* stream);
+
+/*
  * (a4) Sampler policy on given pools ("Speculative decoding on RDNA" §03):
  * pool_vals [rows][64] in pool order, pool_len valid entries per row.
  * All arithmetic is IEEE float32, each operation rounded to nearest, sums

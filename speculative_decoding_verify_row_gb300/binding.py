@@ -38,6 +38,7 @@ VR_MAX_WINDOW_ROWS = 64
 VR_MAX_ROWS = 1024
 VR_MAX_PENALTY_WINDOW = 512
 VR_MAX_REQUESTS = 256
+VR_NOALLOC_SELECT_MAX_ROWS = 32
 
 
 class VerifyRowError(RuntimeError):
@@ -96,6 +97,7 @@ _SIGNATURES = {
     "vr_verify_penalize": ([_P, _I, _I, _P, _P, _I, _P, _I, ctypes.POINTER(vr_policy), _P, _P,
                             _P, _SZ, _P], _I),
     "vr_verify_select": ([_P, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "vr_verify_select_noalloc": ([_P, _I, _I, _P, _P, _P], _I),
     "vr_verify_policy": ([_P, _I, _I, ctypes.POINTER(vr_policy), _P, _P, _P, _P], _I),
     "vr_verify_sample_accept": ([_P, _I, _I, _P, _P, _I, _P, _P, ctypes.POINTER(vr_policy),
                                  _U64, _U64, _P, _P, _P, _P, _SZ, _P], _I),
@@ -219,6 +221,20 @@ def verify_select(logits, pool_ids, pool_vals, ws, stream=None):
     _dev(pool_vals, torch.float32, "pool_vals", (R, VR_POOL))
     _check(lib().vr_verify_select(_ptr(logits), R, V, _ptr(pool_ids), _ptr(pool_vals), _ptr(ws),
                                   ws.numel(), _stream(stream, logits.device)), "vr_verify_select")
+    return pool_ids, pool_vals
+
+
+def verify_select_noalloc(logits, pool_ids, pool_vals, stream=None):
+    """vr_verify_select without a workspace: for callers that cannot give
+    the library device memory; its scratch is a fixed array inside the
+    library, shared by all calls on a device (serialise them)."""
+    R, V = logits.shape
+    _dev(logits, torch.float32, "logits")
+    _dev(pool_ids, torch.int32, "pool_ids", (R, VR_POOL))
+    _dev(pool_vals, torch.float32, "pool_vals", (R, VR_POOL))
+    _check(lib().vr_verify_select_noalloc(_ptr(logits), R, V, _ptr(pool_ids), _ptr(pool_vals),
+                                          _stream(stream, logits.device)),
+           "vr_verify_select_noalloc")
     return pool_ids, pool_vals
 
 

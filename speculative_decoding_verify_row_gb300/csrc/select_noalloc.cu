@@ -1,0 +1,69 @@
+// vr_verify_select_noalloc: the candidate-pool select with its scratch
+// compiled into the library instead of taken from a caller's workspace.
+//
+// Who needs it: callers that cannot hand the library device memory of its
+// own.  Examples are a plugin whose host application owns every device
+// allocation through its own pool and offers no hook to borrow from it, or a
+// process that must not grow its device footprint after start-up.  Such a
+// caller still owns the inputs and outputs; only the select's intermediate
+// candidates need a home, and here they live in one fixed array that every
+// GPU loading this library reserves until the process exits.
+//
+// Rules of use (also stated in include/verifyrow.h):
+//   * rows <= VR_NOALLOC_SELECT_MAX_ROWS; any vocab (the select never splits a
+//     row into more than 80 segments of candidates);
+//   * the array is shared by every call on a device and keeps the last
+//     call's contents; calls that overlap on the GPU (two streams, or two
+//     host threads) race on it and must be serialised by the caller;
+//   * nothing in it needs to start at zero: the first phase of the select
+//     writes every candidate slot that the second phase reads;
+//   * the first call on each device looks up the array's device address
+//     (cudaGetSymbolAddress with that device current) and remembers it, so
+//     make that first call before any stream capture on that device.
+#include <mutex>
+
+#include "vr_common.cuh"
+#include "vr_kernels.h"
+
+namespace vr {
+namespace {
+
+constexpr int kNoallocMaxSegments = 80;
+constexpr size_t kNoallocSlots =
+    static_cast<size_t>(VR_NOALLOC_SELECT_MAX_ROWS) * kNoallocMaxSegments * kPool;
+
+// 32 rows x 80 segments x 64 candidates x 8 bytes = 1.25 MiB
+static __device__ __align__(256) uint64_t g_select_scratch[kNoallocSlots];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+uint64_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once
+// per device); nullptr on failure.
+uint64_t* scratch_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) return nullptr;
+    g_scratch_ptr[dev] = static_cast<uint64_t*>(p);
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace vr
+
+extern "C" int vr_verify_select_noalloc(const float* logits, int rows, int vocab,
+                                        int32_t* pool_ids, float* pool_vals, void* stream) {
+  if (!logits || !pool_ids || !pool_vals || rows < 1 || vocab < 1) return VR_ERR_ARG;
+  if (rows > VR_NOALLOC_SELECT_MAX_ROWS) return VR_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(rows) * vr::select_segments(vocab) * vr::kPool > vr::kNoallocSlots)
+    return VR_ERR_UNSUPPORTED;
+  uint64_t* scratch = vr::scratch_for_current_device();
+  if (!scratch) return VR_ERR_CUDA;
+  return vr::launch_select(logits, rows, vocab, scratch, pool_ids, pool_vals, nullptr, nullptr,
+                           static_cast<cudaStream_t>(stream));
+}
