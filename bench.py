@@ -46,6 +46,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the penalised-chain, tree and batched workloads")
     p.add_argument("--mode", choices=["full", "window", "project"], default="full",
                    help="window: only the timed windows (for a profiler's launch list); "
                         "project: only the projection of one window (for a kernel capture)")
@@ -217,6 +219,124 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _event_time(torch, stream, fn, n):
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    for i in range(3):
+        fn(i)
+    t0.record(stream)
+    for i in range(n):
+        fn(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / 1000.0 / n
+
+
+def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
+    """The other verify workloads on the same GPU: the penalised chain (k 8),
+    the 3 x 8 token tree (greedy and sampled) and 64 batched requests at
+    hidden 5120.  Per-window time of the fused call, events on the stream;
+    inputs resident, 32 distinct windows cycled."""
+    out = {}
+    w_bf16 = wd.view(torch.bfloat16)
+    nwin = 32
+
+    def top32(a):                              # [R, H] -> cuBLAS bf16 top-32 (input prep)
+        lg = (a.to(torch.bfloat16) @ w_bf16.T).float()
+        v, i = torch.topk(lg, 32, dim=1)
+        return i.cpu().numpy(), v.cpu().numpy()
+
+    # penalised chain: k 8, W 64, repeat 1.1, presence 1.5, frequency 0.2, top-k 0
+    k, R = 8, 9
+    pol = vb.Policy(temperature=0.7, top_k=0, min_p=0.05, top_p=0.95, repeat=1.1, presence=1.5,
+                    frequency=0.2, window=64)
+    wins = []
+    for s in range(nwin):
+        a = torch.from_numpy(synth.activations(R, H, 100 + s)).to(dev)
+        ti, tv = top32(a[:k])
+        qi, ql = synth.draft_candidates(ti, tv, seed=100 + s)
+        slot = synth.draft_choice(ql, 0.7, seed=101 + s)
+        wins.append(dict(a=a, q=torch.from_numpy(qi).to(dev), ql=torch.from_numpy(ql).to(dev),
+                         d=torch.from_numpy(qi[np.arange(k), slot].astype(np.int32)).to(dev),
+                         h=torch.from_numpy(synth.zipf_history(4096, V, seed=100 + s)).to(dev)))
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    pen = torch.empty_like(lg)
+    o = torch.empty(R, dtype=torch.int32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    ne = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = vb.workspace(R, H, V, device=dev)
+
+    def pen_window(i):
+        w = wins[i % nwin]
+        vb.verify_window(wd, w["a"], w["d"], pol, i, 4096, lg, o, acc, ne, ws, q_ids=w["q"],
+                         q_logits=w["ql"], hist=w["h"], pen_logits=pen, stream=stream)
+    t = _event_time(torch, stream, pen_window, n_steps)
+    out["penalised_chain_k8"] = {"windows_per_s": 1.0 / t, "us_per_window": 1e6 * t, "rows": R}
+
+    # token tree: 3 branches x depth 8 (25 rows)
+    parent = torch.from_numpy(synth.tree_parents(3, 8)).to(dev)
+    R = 25
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    pen = torch.empty_like(lg)
+    o = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = vb.workspace(R, H, V, device=dev)
+    twins = []
+    for s in range(nwin):
+        a = torch.from_numpy(synth.activations(R, H, 200 + s)).to(dev)
+        ti, _ = top32(a)
+        toks = synth.tree_tokens(ti[:, 0], ti, seed=200 + s)
+        twins.append(dict(a=a, t=torch.from_numpy(toks).to(dev),
+                          h=torch.from_numpy(synth.zipf_history(2048, V, seed=200 + s)).to(dev)))
+    for name, tpol in (("tree_3x8_greedy", vb.Policy()),
+                       ("tree_3x8_sampled", vb.Policy(temperature=0.7, top_k=20, presence=1.5,
+                                                      window=64))):
+        def tree_window(i, tpol=tpol):
+            w = twins[i % nwin]
+            vb.verify_window(wd, w["a"], w["t"], tpol, i, 2048, lg, o, acc, ne, ws, parent=parent,
+                             hist=w["h"], pen_logits=pen, stream=stream)
+        t = _event_time(torch, stream, tree_window, n_steps)
+        out[name] = {"windows_per_s": 1.0 / t, "us_per_window": 1e6 * t, "rows": R}
+    del wins, twins, lg, pen, ws
+
+    # batched serving: 64 requests x k 3 at hidden 5120
+    H5, nreq, k = 5120, 64, 3
+    W5 = synth.weights(V, H5)
+    wd5 = torch.from_numpy(W5.view(np.int16)).to(dev)
+    del W5
+    R = nreq * (k + 1)
+    A = torch.from_numpy(synth.activations(R, H5, 500)).to(dev)
+    rng = np.random.default_rng(500)
+    keep, reqs = [], []
+    for b in range(nreq):
+        greedy = b % 2 == 0
+        bpol = vb.Policy() if greedy else vb.Policy(temperature=0.8, top_k=20, top_p=0.9,
+                                                     presence=1.5, window=64)
+        qi = rng.integers(0, V, (k, 8)).astype(np.int32)
+        ql = rng.standard_normal((k, 8)).astype(np.float32)
+        t = dict(d=torch.from_numpy(qi[:, 0].copy()).to(dev), q=torch.from_numpy(qi).to(dev),
+                 ql=torch.from_numpy(ql).to(dev),
+                 h=torch.from_numpy(synth.zipf_history(2048, V, seed=1000 + b)).to(dev),
+                 o=torch.empty(k + 1, dtype=torch.int32, device=dev),
+                 a=torch.empty(1, dtype=torch.int32, device=dev),
+                 n=torch.empty(1, dtype=torch.int32, device=dev))
+        keep.append(t)
+        reqs.append(vb.make_request(k, t["d"], bpol, b, 2048, t["o"], t["a"], t["n"], q_ids=t["q"],
+                                    q_logits=t["ql"], hist=t["h"]))
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    pen = torch.empty_like(lg)
+    ws = vb.workspace(R, H5, V, device=dev)
+
+    def batched(i):
+        vb.verify_window_batched(wd5, A, reqs, lg, ws, pen_logits=pen, stream=stream)
+    t = _event_time(torch, stream, batched, max(5, n_steps // 50))
+    flops = 2.0 * R * H5 * V
+    out["batched_64x4_h5120"] = {"windows_per_s": nreq / t, "us_per_call": 1e6 * t, "rows": R,
+                                 "algorithmic_tflops": flops / t / 1e12,
+                                 "weight_gbs": V * H5 * 2 / t / 1e9}
+    del wd5
+    return out
+
+
 def run_projection_only(torch, vb, synth, wd, dev, args):
     """The projection of one 4-row window, warm-up + steps times."""
     a = torch.from_numpy(synth.activations(ROWS, H, 0)).to(dev)
@@ -348,6 +468,9 @@ def main():
             torch.cuda.synchronize(dev)
             sweep[name][str(R)] = round(1000.0 * t0.elapsed_time(t1) / n_it, 2)
 
+    extra = None if args.no_extra else extra_workloads(torch, vb, synth, wd, dev, stream,
+                                                       min(args.steps, 1000))
+
     # ---- e2e: host inputs -> window -> host outputs, through the C ABI ----
     pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
     h_act = [pin(win["act_np"][s]) for s in range(N_WINDOWS)]
@@ -393,6 +516,7 @@ def main():
                       "pool_select_only": select_us,
                       "window": 1e6 * job_s / args.steps},
         "rows_sweep_us": sweep,
+        "other_workloads": extra,
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_units / e2e_job_s, "unit": "windows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -180,8 +180,10 @@ VR_API int vr_verify_select(const float* logits, int rows, int vocab, int32_t* p
  * of its own (for example a plugin whose host application owns every device
  * allocation, or a process that must not grow its device footprint after
  * start-up).  Same inputs, outputs and results as vr_verify_select; the
- * select's intermediate candidates live in a fixed 1.25 MiB array compiled
- * into the library, which every GPU that loads the library keeps until exit.
+ * select's intermediate candidates and its row counters live in a fixed
+ * 1 MiB array compiled into the library, which every GPU that loads the
+ * library keeps until exit.  Each call clears the counters with an
+ * asynchronous memset on `stream` before its kernel.
  * Limits and rules:
  *   - rows <= VR_NOALLOC_SELECT_MAX_ROWS (else VR_ERR_UNSUPPORTED); any vocab;
  *   - the array is shared by all calls on a device and keeps the last call's
@@ -295,8 +297,9 @@ VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int
 VR_API int vr_device_status(void* ws, int32_t* out_status, void* stream);
 
 /*
- * Zero-initialise a fresh workspace (the status word).  Call once after
- * allocating ws; enqueued on `stream`.
+ * Zero-initialise a fresh workspace: its first 8 KiB hold the status word
+ * and the ticket counters of the sampling kernel (which leaves them at zero
+ * after every call).  Call once after allocating ws; enqueued on `stream`.
  */
 VR_API int vr_workspace_init(void* ws, size_t ws_bytes, void* stream);
 

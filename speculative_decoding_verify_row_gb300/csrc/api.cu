@@ -11,6 +11,13 @@ namespace vr {
 namespace {
 
 constexpr size_t kAlign = 256;
+// control region at the start of every workspace, zeroed by vr_workspace_init:
+// the status word, then the per-row and per-request ticket counters of the
+// sampling kernel (which leaves them at zero after every call)
+constexpr size_t kRowTicketOff = 256;
+constexpr size_t kReqTicketOff = kRowTicketOff + VR_MAX_ROWS * 4;
+constexpr size_t kControlBytes = 8192;
+static_assert(kReqTicketOff + VR_MAX_REQUESTS * 4 <= kControlBytes, "control region");
 
 struct Layout {
   size_t status, planes, cand, pool_ids, pool_vals, dec, q_pen, reqs, row_req;
@@ -26,7 +33,7 @@ Layout layout(int rows, int hidden, int vocab) {
     return at;
   };
   const size_t r = static_cast<size_t>(rows);
-  L.status = take(kAlign);
+  L.status = take(kControlBytes);
   L.planes = take(tc_plane_bytes(rows, hidden));
   L.cand = take(select_cand_bytes(rows, vocab));
   L.pool_ids = take(r * kPool * 4);
@@ -143,10 +150,12 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
     st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);
     if (st != VR_OK) return st;
   }
-  st = launch_select(target, rows, vocab, at<uint64_t>(ws, L.cand), at<int32_t>(ws, L.pool_ids),
-                     at<float>(ws, L.pool_vals), &tab, at<int4>(ws, L.dec), s);
-  if (st != VR_OK) return st;
-  return launch_accept(tab, n_req, vocab, at<int4>(ws, L.dec), at<int32_t>(ws, L.status), s);
+  (void)n_req;
+  return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
+                       at<uint32_t>(ws, L.status + kRowTicketOff),
+                       at<uint32_t>(ws, L.status + kReqTicketOff), at<int32_t>(ws, L.pool_ids),
+                       at<float>(ws, L.pool_vals), &tab, at<int4>(ws, L.dec),
+                       at<int32_t>(ws, L.status), s);
 }
 
 int window_device(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
@@ -201,8 +210,9 @@ int vr_workspace_bytes(int rows, int hidden, int vocab, size_t* out_bytes) {
 }
 
 int vr_workspace_init(void* ws, size_t ws_bytes, void* stream) {
-  if (!ws || ws_bytes < kAlign || reinterpret_cast<uintptr_t>(ws) % kAlign) return VR_ERR_WORKSPACE;
-  return cudaMemsetAsync(ws, 0, kAlign, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  if (!ws || ws_bytes < kControlBytes || reinterpret_cast<uintptr_t>(ws) % kAlign)
+    return VR_ERR_WORKSPACE;
+  return cudaMemsetAsync(ws, 0, kControlBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? VR_OK
              : VR_ERR_CUDA;
 }
@@ -243,8 +253,10 @@ int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids
   if (!logits || !pool_ids || !pool_vals) return VR_ERR_ARG;
   if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
   const Layout L = layout(rows, 8, vocab);
-  return launch_select(logits, rows, vocab, at<uint64_t>(ws, L.cand), pool_ids, pool_vals,
-                       nullptr, nullptr, static_cast<cudaStream_t>(stream));
+  return launch_sample(logits, rows, vocab, at<uint64_t>(ws, L.cand),
+                       at<uint32_t>(ws, L.status + kRowTicketOff),
+                       at<uint32_t>(ws, L.status + kReqTicketOff), pool_ids, pool_vals, nullptr,
+                       nullptr, at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,

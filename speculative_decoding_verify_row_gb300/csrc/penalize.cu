@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(THREADS)
   __shared__ int32_t path[VR_MAX_WINDOW_ROWS];
   __shared__ int h_len, bad;
 
+  pdl_trigger();
+  pdl_wait();
   const bool is_q = blockIdx.x >= static_cast<unsigned>(rows_total);
   const int g = is_q ? blockIdx.x - rows_total : blockIdx.x;   // global row
   const ReqDev& rq = request(tab, request_of_row(tab, g));
@@ -109,6 +111,8 @@ __global__ void __launch_bounds__(THREADS)
 // Copy the given candidate logits into the workspace copy unchanged (the
 // penalty kernel only rewrites them when penalties are active).
 __global__ void copy_q_kernel(ReqTable tab, int rows_total) {
+  pdl_trigger();
+  pdl_wait();
   const int g = blockIdx.x;
   const ReqDev& rq = request(tab, request_of_row(tab, g));
   const int local = g - rq.row0;
@@ -122,11 +126,14 @@ __global__ void copy_q_kernel(ReqTable tab, int rows_total) {
 
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab, bool with_q,
                     int32_t* status, cudaStream_t stream) {
-  if (with_q) pen::copy_q_kernel<<<rows_total, 32, 0, stream>>>(tab, rows_total);
+  if (with_q && launch_pdl(pen::copy_q_kernel, dim3(rows_total), dim3(32), 0, stream, tab,
+                          rows_total) != cudaSuccess)
+    return VR_ERR_CUDA;
   const int blocks = rows_total * (with_q ? 2 : 1);
-  pen::penalize_kernel<<<blocks, pen::THREADS, 0, stream>>>(tab, rows_total, logits, vocab,
-                                                            with_q ? 1 : 0, status);
-  return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;
+  return launch_pdl(pen::penalize_kernel, dim3(blocks), dim3(pen::THREADS), 0, stream, tab,
+                    rows_total, logits, vocab, with_q ? 1 : 0, status) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
 }
 
 }  // namespace vr

@@ -31,11 +31,20 @@ constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
 constexpr int MAX_SMEM = 200 * 1024;
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+// Weights are read once per call: no L1 allocation, and evict-first in L2 so
+// that the stream does not push the logits, activations or the next
+// kernels' code out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p, uint64_t policy) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(policy));
   return v;
 }
 
@@ -47,6 +56,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     project_ffma_kernel(const uint16_t* __restrict__ weight, const float* __restrict__ act,
                         int hidden, int vocab, int row_base, float* __restrict__ logits) {
   extern __shared__ float4 sA[];               // [2][RB][chunks]
+  pdl_trigger();
+  pdl_wait();
   const int chunks = hidden / 8;
   float4* sLo = sA;
   float4* sHi = sA + RB * chunks;
@@ -61,6 +72,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int steps = (chunks + 31) / 32;
+  const uint64_t pol = l2_policy_evict_first();
   const long long n_tasks = (static_cast<long long>(vocab) + NV - 1) / NV;
   const long long gw = static_cast<long long>(blockIdx.x) * WARPS + warp;
   const long long tw = static_cast<long long>(gridDim.x) * WARPS;
@@ -84,7 +96,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     {
       const int c = lane;
 #pragma unroll
-      for (int n = 0; n < NV; ++n) cur[n] = (c < chunks) ? ld_stream(wrow[n] + c) : make_uint4(0, 0, 0, 0);
+      for (int n = 0; n < NV; ++n) cur[n] = (c < chunks) ? ld_stream(wrow[n] + c, pol) : make_uint4(0, 0, 0, 0);
     }
     for (int j = 0; j < steps; ++j) {
       const int c = lane + 32 * j;
@@ -92,7 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint4 nxt[NV];
 #pragma unroll
       for (int n = 0; n < NV; ++n)
-        nxt[n] = (j + 1 < steps && cn < chunks) ? ld_stream(wrow[n] + cn) : make_uint4(0, 0, 0, 0);
+        nxt[n] = (j + 1 < steps && cn < chunks) ? ld_stream(wrow[n] + cn, pol) : make_uint4(0, 0, 0, 0);
       if (c < chunks) {
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
@@ -150,9 +162,10 @@ int launch_pass(const uint16_t* weight, const float* act, int hidden, int vocab,
   if (cudaFuncSetAttribute(project_ffma_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return VR_ERR_CUDA;
-  project_ffma_kernel<RB><<<sms, THREADS, smem, stream>>>(weight, act, hidden, vocab, row_base,
-                                                         logits);
-  return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;
+  return launch_pdl(project_ffma_kernel<RB>, dim3(sms), dim3(THREADS), smem, stream, weight, act,
+                    hidden, vocab, row_base, logits) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
 }
 
 }  // namespace ffma

@@ -100,12 +100,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return true;
 }
 
+// L2 policies: the weights are streamed once per window and must not push
+// anything else out of L2 (the logits the next kernel reads, the planes every
+// CTA re-reads, the code and scratch of the sampling stage), so they are
+// loaded evict-first; the plane tiles, shared by all CTAs, evict-last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -207,10 +222,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the prologue above overlaps the previous kernel; from here on the planes
+  // and the logits buffer are touched, so wait for it to complete
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0) {
     // ---------------- producer: TMA ring ----------------
     if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
       int last_fill_parity[STAGES];
@@ -224,8 +245,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t* st = smem + s * STAGE_BYTES;
           for (int mt = 0; mt < nmt; ++mt)
             tma_load_2d(smem_u32(st + mt * W_TILE_BYTES), &tm_w, kb * BK, (u * MT + mt) * BM,
-                        full_bar(s));
-          tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_b, kb * BK, 0, full_bar(s));
+                        full_bar(s), pol_w);
+          tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_b, kb * BK, 0, full_bar(s), pol_b);
           last_fill_parity[s] = static_cast<int>(ph);
           if (++s == STAGES) {
             s = 0;
@@ -349,6 +370,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 // mid = RN(a - hi), lo = RN(a - hi - mid); both subtractions are exact.
 __global__ void split_planes_kernel(const float* __restrict__ act, int rows, int hidden,
                                     int groups, __nv_bfloat16* __restrict__ planes) {
+  pdl_trigger();
+  pdl_wait();
   const int chunks = hidden / 8;
   const long long total = static_cast<long long>(groups) * NP * chunks;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -441,7 +464,9 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
     const int threads = 256;
     const int blocks = static_cast<int>(std::min<long long>((work + threads - 1) / threads,
                                                             static_cast<long long>(g_num_sms) * 8));
-    tc::split_planes_kernel<<<blocks, threads, 0, stream>>>(act, rows, hidden, groups, pl);
+    if (launch_pdl(tc::split_planes_kernel, dim3(blocks), dim3(threads), 0, stream, act, rows,
+                   hidden, groups, pl) != cudaSuccess)
+      return VR_ERR_CUDA;
   }
   CUtensorMap tm_w;
   if (!encode_bf16_2d(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
@@ -454,8 +479,9 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
                         tc::BK, tc::BN))
       return VR_ERR_ARG;
     const int rg = std::min(tc::NP, rows - g * tc::NP);
-    tc::project_tc_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, stream>>>(
-        tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, status);
+    if (launch_pdl(tc::project_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
+                   tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, status) != cudaSuccess)
+      return VR_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;
 }

@@ -1,0 +1,624 @@
+// The sampling stage of a verify window, in one kernel: candidate pools,
+// sampler policy, per-row random decisions and acceptance.
+//
+// Pool ("Speculative decoding on RDNA" §03: a 64-wide pool with a fixed tie
+// order; "feat(dflash) ...": a top-K select held to byte identity with ties,
+// NaN and -inf).  Each entry of a row becomes one 64-bit composite,
+// (order key << 32) | ~id, whose unsigned order is the pool order (value
+// descending, token id ascending, NaN lowest, -0.0 below +0.0), so the top-64
+// set is unique.
+//
+// Grid (segments, rows), no CTA ever waits for another:
+//  1. every CTA reduces its segment of one row to the segment's top 64 by a
+//     block radix select and stores them in pool order;
+//  2. it takes a ticket on the row's counter; the CTA that draws the last
+//     ticket has every segment list of the row available, merges them
+//     pairwise (merge path) into the row's pool, applies the sampler policy
+//     and takes every random decision of the row (emit draw, accept test,
+//     residual draw), and resets the counter;
+//  3. that CTA then takes a ticket on the request's counter; the last row of
+//     the request to finish walks the request's rows and writes the emitted
+//     ids (greedy prefix or longest tree branch, §02; rejection sampling,
+//     §03 steps 1-4; naive descent for deterministic tree drafts, "feat(dflash)
+//     ...").
+// Tickets follow a __threadfence() after the CTA's writes, so the last CTA
+// sees all of them (the usual threadfence-reduction pattern).
+#include <algorithm>
+
+#include "vr_common.cuh"
+#include "vr_kernels.h"
+
+namespace vr {
+namespace smp {
+
+constexpr int THREADS = 256;
+constexpr int SUB = 4096;                    // entries per sub-block of a segment
+constexpr int ITEMS = SUB / THREADS + 1;     // + one carried candidate (threads < 64)
+constexpr int MAX_SEG = 64;
+constexpr int NPASS = 6;
+__constant__ int kDigitBits[NPASS] = {12, 12, 8, 12, 12, 8};   // 64 bits, most significant first
+constexpr int MAX_BINS = 4096;
+constexpr int GATHER_MAX = THREADS;
+constexpr int MAXR = VR_MAX_WINDOW_ROWS;
+
+struct SelectShared {
+  uint32_t hist[MAX_BINS];
+  uint64_t gather[GATHER_MAX];
+  uint64_t out[kPool];
+  uint32_t warp_sum[THREADS / 32];
+  int count, gcount, digit, above, n_valid;
+};
+
+struct MergeShared {
+  uint64_t in[MAX_SEG][kPool];
+  uint64_t out[MAX_SEG / 2][kPool];
+};
+
+union StageShared {
+  SelectShared sel;
+  MergeShared mrg;
+};
+
+struct RowShared {
+  float e[kPool], pc[kPool], r[kPool], pr[kPool];
+  float qe[kPool], qp[kQCand];
+  float vals[kPool], qv[kQCand];
+  int32_t ids[kPool], qid[kQCand];
+  int m, qm, chain, acc;
+  float S, qS;
+};
+
+struct AcceptShared {
+  int32_t tok[MAXR], par[MAXR];
+  int4 d[MAXR];
+  int bad, not_chain;
+};
+
+// ---------------------------------------------------------------------------
+// block radix select
+
+// Find the bin holding the need-th largest entry, bins walked from the top.
+// Warp w owns the bins [nb - (w+1) nb/8, nb - w nb/8); its lanes read them
+// in 32-bin chunks with consecutive lanes on consecutive bins (no bank
+// conflicts), a warp scan turns each chunk into running counts, and the
+// warps' totals give each warp the count of everything above its range.
+__device__ __forceinline__ void find_digit(int nb, int need, SelectShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_warp = nb / (THREADS / 32);
+  const int top = nb - warp * per_warp;
+  uint32_t total = 0;
+  for (int c = 0; c < per_warp; c += 32) total += sh.hist[top - 1 - c - lane];
+  total = __reduce_add_sync(0xffffffffu, total);
+  if (lane == 0) sh.warp_sum[warp] = total;
+  __syncthreads();
+  uint32_t cum = 0;
+  for (int w = 0; w < warp; ++w) cum += sh.warp_sum[w];
+  if (cum < static_cast<uint32_t>(need) && cum + total >= static_cast<uint32_t>(need)) {
+    for (int c = 0; c < per_warp; c += 32) {
+      const int b = top - 1 - c - lane;          // lane 0 holds the highest bin
+      const uint32_t h = sh.hist[b];
+      uint32_t incl = h;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t before = cum + incl - h;
+      if (before < static_cast<uint32_t>(need) && before + h >= static_cast<uint32_t>(need)) {
+        sh.digit = b;
+        sh.above = static_cast<int>(before);
+      }
+      cum += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// Top-64 of the nonzero composites held by the block (ITEMS per thread),
+// left in no particular order in sh.out[0..sh.count).  Radix select, most
+// significant digit first (12-bit first digit, so a row's largest values
+// spread over many bins); once the entries that tie with the resolved prefix
+// are few (<= 256) they are gathered and the rest is decided by rank
+// counting; if they are exactly the ones still needed, all are taken.
+__device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) mine += (x[i] != 0ull);
+  if (tid == 0) {
+    sh.n_valid = 0;
+    sh.count = 0;
+    sh.gcount = 0;
+  }
+  __syncthreads();
+  mine = __reduce_add_sync(0xffffffffu, mine);
+  if (lane == 0) atomicAdd(&sh.n_valid, mine);
+  __syncthreads();
+
+  uint64_t prefix = 0ull, mask = 0ull;
+  bool gathered = false;
+  int need = kPool;
+  if (sh.n_valid > kPool) {
+    int shift = 64;
+    for (int pass = 0; pass < NPASS; ++pass) {
+      const int bits = kDigitBits[pass];
+      const int nb = 1 << bits;
+      shift -= bits;
+      for (int b = tid; b < nb; b += THREADS) sh.hist[b] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i)
+        if (x[i] != 0ull && (x[i] & mask) == prefix)
+          atomicAdd(&sh.hist[static_cast<uint32_t>(x[i] >> shift) & (nb - 1)], 1u);
+      __syncthreads();
+      find_digit(nb, need, sh);
+      const int d = sh.digit;
+      need -= sh.above;
+      prefix |= static_cast<uint64_t>(d) << shift;
+      mask |= static_cast<uint64_t>(nb - 1) << shift;
+      const int tie = static_cast<int>(sh.hist[d]);
+      __syncthreads();
+      if (tie == need) break;                 // every tying entry is taken
+      if (tie <= GATHER_MAX) {
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i)
+          if (x[i] != 0ull && (x[i] & mask) == prefix) sh.gather[atomicAdd(&sh.gcount, 1)] = x[i];
+        __syncthreads();
+        gathered = true;
+        break;
+      }
+    }
+  }
+  if (!gathered) {
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+      if (x[i] != 0ull && (x[i] & mask) >= prefix) sh.out[atomicAdd(&sh.count, 1)] = x[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+      if (x[i] != 0ull && (x[i] & mask) > prefix) sh.out[atomicAdd(&sh.count, 1)] = x[i];
+    const int g = sh.gcount;
+    if (tid < g) {
+      const uint64_t me = sh.gather[tid];
+      int rank = 0;
+      for (int j = 0; j < g; ++j) rank += (sh.gather[j] > me);
+      if (rank < need) sh.out[atomicAdd(&sh.count, 1)] = me;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint64_t composite_at(const float* row, long long e) {
+  return pack_key_id(float_key(row[e]), static_cast<uint32_t>(e));
+}
+
+// ---------------------------------------------------------------------------
+// merge of sorted lists
+
+// The (k+1)-th largest of two descending lists of 64 distinct nonzero
+// composites padded with zeros: merge path, i.e. the number i of entries
+// that come from a among the first k outputs, found by binary search.
+__device__ __forceinline__ uint64_t merged_at(const uint64_t* a, const uint64_t* b, int k) {
+  int lo = k > kPool ? k - kPool : 0, hi = k < kPool ? k : kPool;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] > b[k - 1 - mid]) lo = mid + 1;
+    else hi = mid;
+  }
+  const int i = lo;
+  return (i < kPool && (k - i >= kPool || a[i] > b[k - i])) ? a[i] : b[k - i];
+}
+
+// Merge the row's nseg sorted lists (each the top 64 of its segment) into
+// the row's top 64: the top 64 of the union of two lists is the top 64 of
+// their merge, so merging pairs until one list is left gives the pool.
+// Returns the final list (shared memory).
+__device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeShared& ms) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < nseg * kPool; i += THREADS) ms.in[i / kPool][i % kPool] = lists[i];
+  __syncthreads();
+  uint64_t(*src)[kPool] = ms.in;
+  uint64_t(*dst)[kPool] = ms.out;
+  int nl = nseg;
+  while (nl > 1) {
+    const int pairs = nl >> 1;
+    for (int i = tid; i < pairs * kPool; i += THREADS) {
+      const int p = i / kPool, k = i % kPool;
+      dst[p][k] = merged_at(src[2 * p], src[2 * p + 1], k);
+    }
+    if (nl & 1)
+      for (int k = tid; k < kPool; k += THREADS) dst[pairs][k] = src[nl - 1][k];
+    __syncthreads();
+    uint64_t(*t)[kPool] = src;
+    src = dst;
+    dst = t;
+    nl = pairs + (nl & 1);
+  }
+  return src[0];
+}
+
+// ---------------------------------------------------------------------------
+// per-row decisions
+
+__device__ __forceinline__ int first_above(const float* c, int m, float t) {
+  // smallest j < m with c[j] > t, c non-decreasing; -1 if none
+  const int lane = threadIdx.x & 31;
+  uint32_t b = __ballot_sync(0xffffffffu, lane < m && c[lane] > t);
+  if (b) return __ffs(b) - 1;
+  b = __ballot_sync(0xffffffffu, lane + 32 < m && c[lane + 32] > t);
+  return b ? 32 + __ffs(b) - 1 : -1;
+}
+
+__device__ __forceinline__ int last_positive(const float* w, int m) {
+  const int lane = threadIdx.x & 31;
+  uint32_t b = __ballot_sync(0xffffffffu, lane + 32 < m && w[lane + 32] > 0.0f);
+  if (b) return 32 + 31 - __clz(b);
+  b = __ballot_sync(0xffffffffu, lane < m && w[lane] > 0.0f);
+  return b ? 31 - __clz(b) : 0;
+}
+
+// All random decisions of one row, taken from its pool (rs.ids/rs.vals, n
+// entries) by the whole CTA; writes dec[row] = (argmax, emit draw y,
+// residual draw z, accept bit):
+//   y: the draw from p with u(row, emit);
+//   z: rows that verify a chain draft with candidates: the draw from
+//      (p - q)+ renormalised with the same uniform (y if that is all zero);
+//   acc: u(row, accept) * q(x) < p(x) for the row's draft x (q(x) = 0:
+//      p(x) > 0).
+__device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4* dec) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const vr_policy& pol = rq.pol;
+  const int local = row - rq.row0;
+  if (pol.temperature == 0.f) {
+    if (tid == 0) dec[row] = make_int4(rs.ids[0], rs.ids[0], rs.ids[0], 0);
+    return;
+  }
+  if (tid == 0) rs.chain = 1;
+  __syncthreads();
+  if (rq.parent)
+    for (int j = tid; j < rq.n_nodes; j += THREADS)
+      if (rq.parent[j] != j - 1) rs.chain = 0;
+  __syncthreads();
+  const bool reject_row = rq.q_ids != nullptr && rs.chain && local < rq.n_nodes;
+  const uint64_t urow = static_cast<uint64_t>(local);
+
+  if (warp == 0) {
+    policy_warp(rs.vals, n, pol, rs.e, &rs.m, &rs.S);
+    if (lane == 0) {
+      float acc = 0.0f;
+      for (int j = 0; j < rs.m; ++j) {
+        acc = __fadd_rn(acc, rs.e[j]);
+        rs.pc[j] = acc;
+      }
+    }
+  } else if (warp == 1 && reject_row) {
+    // q: the node's candidates in pool order, then the same policy
+    const float* qv = rq.q_pen + static_cast<size_t>(local) * kQCand;
+    const int32_t* qi = rq.q_ids + static_cast<size_t>(local) * kQCand;
+    if (lane < kQCand) {
+      const uint32_t k = float_key(qv[lane]);
+      const int32_t id = qi[lane];
+      int rank = 0;
+      for (int s2 = 0; s2 < kQCand; ++s2) {
+        const uint32_t ks = float_key(qv[s2]);
+        const int32_t is = qi[s2];
+        rank += (ks > k) || (ks == k && (is < id || (is == id && s2 < lane)));
+      }
+      rs.qid[rank] = id;
+      rs.qv[rank] = qv[lane];
+    }
+    __syncwarp();
+    policy_warp(rs.qv, kQCand, pol, rs.qe, &rs.qm, &rs.qS);
+    if (lane < rs.qm) rs.qp[lane] = __fdiv_rn(rs.qe[lane], rs.qS);
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  const int m = rs.m;
+  const float S = rs.S;
+  const float u2 = uniform01(rq.seed, rq.position, urow, kPurposeEmit);
+  int j = first_above(rs.pc, m, __fmul_rn(u2, S));
+  if (j < 0) j = last_positive(rs.e, m);
+  const int32_t y = rs.ids[j];
+  int32_t z = y;
+  int acc = 0;
+  if (reject_row) {
+    const int32_t xd = rq.tokens[local];
+    const int qm = rs.qm;
+    float px = 0.0f;
+    for (int jj = lane; jj < m; jj += 32) {
+      const float pj = __fdiv_rn(rs.e[jj], S);
+      float qj = 0.0f;
+      for (int s2 = 0; s2 < qm; ++s2)
+        if (rs.qid[s2] == rs.ids[jj]) qj = __fadd_rn(qj, rs.qp[s2]);
+      const float d = __fsub_rn(pj, qj);
+      rs.r[jj] = d > 0.0f ? d : 0.0f;
+      if (rs.ids[jj] == xd) px = pj;
+    }
+    // pool ids are distinct: at most one lane holds p(x)
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float other = __shfl_xor_sync(0xffffffffu, px, o);
+      px = other != 0.0f ? other : px;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      float qx = 0.0f;
+      for (int s2 = 0; s2 < qm; ++s2)
+        if (rs.qid[s2] == xd) qx = __fadd_rn(qx, rs.qp[s2]);
+      const float u1 = uniform01(rq.seed, rq.position, urow, kPurposeAccept);
+      rs.acc = (qx > 0.0f) ? (__fmul_rn(u1, qx) < px) : (px > 0.0f);
+      float a = 0.0f;
+      for (int jj = 0; jj < m; ++jj) {
+        a = __fadd_rn(a, rs.r[jj]);
+        rs.pr[jj] = a;
+      }
+    }
+    __syncwarp();
+    acc = rs.acc;
+    const float sr = m ? rs.pr[m - 1] : 0.0f;
+    if (sr > 0.0f) {
+      int jz = first_above(rs.pr, m, __fmul_rn(u2, sr));
+      if (jz < 0) jz = last_positive(rs.r, m);
+      z = rs.ids[jz];
+    }
+  }
+  if (lane == 0) dec[row] = make_int4(rs.ids[0], y, z, acc);
+}
+
+// ---------------------------------------------------------------------------
+// acceptance walk of one request (thread 0 writes; the CTA validates)
+
+__device__ void accept_request(const ReqDev& rq, int vocab, const int4* dec, int32_t* status,
+                               AcceptShared& as) {
+  const int n = rq.n_nodes, R = n + 1, tid = threadIdx.x;
+  const bool greedy = rq.pol.temperature == 0.f;
+  if (tid == 0) {
+    as.bad = 0;
+    as.not_chain = 0;
+  }
+  __syncthreads();
+  for (int j = tid; j < R; j += THREADS) as.d[j] = dec[rq.row0 + j];
+  if (tid < n) {
+    const int t = rq.tokens[tid];
+    const int p = rq.parent ? rq.parent[tid] : tid - 1;
+    as.tok[tid] = t;
+    as.par[tid] = p;
+    int b = 0;
+    if (t < 0 || t >= vocab) b |= VR_DEV_BAD_TOKEN;
+    if (p < -1 || p >= tid) b |= VR_DEV_BAD_PARENT;
+    if (p != tid - 1) atomicOr(&as.not_chain, 1);
+    if (b) atomicOr(&as.bad, b);
+  }
+  __syncthreads();
+  const bool rejection = !greedy && rq.q_ids != nullptr && !as.not_chain;
+  if (rejection)
+    for (int i = tid; i < n * kQCand; i += THREADS) {
+      const int id = rq.q_ids[i];
+      if (id < 0 || id >= vocab) atomicOr(&as.bad, VR_DEV_BAD_QID);
+    }
+  __syncthreads();
+  if (tid != 0) return;
+  if (as.bad) {
+    set_status(status, as.bad);
+    *rq.out_accept = 0;
+    *rq.out_n = 0;
+    return;
+  }
+  int32_t* out = rq.out_ids;
+  const int4* d = as.d;
+  int accepted = 0;
+  if (greedy) {
+    bool ok[MAXR];
+    int depth[MAXR];
+    int best = -1, best_depth = 0;
+    for (int j = 0; j < n; ++j) {
+      const int p = as.par[j];
+      ok[j] = as.tok[j] == d[p < 0 ? 0 : 1 + p].x && (p < 0 || ok[p]);
+      depth[j] = p < 0 ? 1 : depth[p] + 1;
+      if (ok[j] && depth[j] > best_depth) {
+        best = j;
+        best_depth = depth[j];
+      }
+    }
+    for (int node = best, k = best_depth - 1; node >= 0; node = as.par[node], --k)
+      out[k] = as.tok[node];
+    out[best_depth] = d[best < 0 ? 0 : 1 + best].x;
+    accepted = best_depth;
+  } else if (rejection) {
+    int a = 0;
+    while (a < n && d[a].w) ++a;
+    for (int i = 0; i < a; ++i) out[i] = as.tok[i];
+    out[a] = (a < n) ? d[a].z : d[n].y;
+    accepted = a;
+  } else {
+    int cur = -1, cnt = 0;
+    while (true) {
+      const int32_t y = d[cur < 0 ? 0 : 1 + cur].y;
+      out[cnt++] = y;
+      int next = -1;
+      for (int j = cur + 1; j < n; ++j)
+        if (as.par[j] == cur && as.tok[j] == y) {
+          next = j;
+          break;
+        }
+      if (next < 0) break;
+      cur = next;
+    }
+    accepted = cnt - 1;
+  }
+  *rq.out_accept = accepted;
+  *rq.out_n = accepted + 1;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+
+struct SampleArgs {
+  const float* logits;     // [rows][vocab] (penalised where penalties apply)
+  int vocab, seg_len, nseg;
+  uint64_t* cand;          // [rows][nseg][64]
+  uint32_t* row_ticket;    // [rows], zero between calls
+  uint32_t* req_ticket;    // [requests], zero between calls
+  int32_t* pool_ids;       // [rows][64]
+  float* pool_vals;        // [rows][64]
+  int4* dec;               // [rows]
+  int32_t* status;
+  int decide;              // 0: pools only
+};
+
+__global__ void __launch_bounds__(THREADS)
+    sample_kernel(SampleArgs a, ReqTable tab) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  StageShared& st = *reinterpret_cast<StageShared*>(dyn_smem);
+  __shared__ RowShared rs;
+  __shared__ AcceptShared as;
+  __shared__ int last;
+  pdl_trigger();
+  pdl_wait();
+  const int seg = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
+  const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
+
+  // 1. the segment's top 64, stored in pool order
+  {
+    SelectShared& sh = st.sel;
+    const long long s0 = static_cast<long long>(seg) * a.seg_len;
+    const long long s1 = std::min<long long>(s0 + a.seg_len, a.vocab);
+    uint64_t carry = 0ull;
+    for (long long b = s0; b < s1; b += SUB) {
+      uint64_t x[ITEMS];
+#pragma unroll
+      for (int i = 0; i < SUB / THREADS; ++i) {
+        const long long e = b + i * THREADS + tid;
+        x[i] = (e < s1) ? composite_at(rp, e) : 0ull;
+      }
+      x[ITEMS - 1] = carry;
+      block_top64(x, sh);
+      carry = (tid < sh.count) ? sh.out[tid] : 0ull;
+      __syncthreads();
+    }
+    if (tid < kPool) {
+      int rank = tid;
+      if (carry != 0ull) {
+        rank = 0;
+        for (int j = 0; j < sh.count; ++j) rank += (sh.out[j] > carry);
+      }
+      a.cand[(static_cast<size_t>(row) * a.nseg + seg) * kPool + rank] = carry;
+    }
+  }
+
+  // 2. the last segment of the row to finish builds the pool and decides
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(&a.row_ticket[row], 1u) == static_cast<uint32_t>(a.nseg - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) a.row_ticket[row] = 0u;
+  const uint64_t* pool =
+      merge_lists(a.cand + static_cast<size_t>(row) * a.nseg * kPool, a.nseg, st.mrg);
+  const int n = a.vocab < kPool ? a.vocab : kPool;
+  if (tid < kPool) {
+    int32_t id = -1;
+    float v = __int_as_float(0x7fffffff);
+    if (tid < n) {
+      id = static_cast<int32_t>(packed_id(pool[tid]));
+      v = rp[id];
+    }
+    a.pool_ids[static_cast<size_t>(row) * kPool + tid] = id;
+    a.pool_vals[static_cast<size_t>(row) * kPool + tid] = v;
+    rs.ids[tid] = id;
+    rs.vals[tid] = v;
+  }
+  if (!a.decide) return;
+  __syncthreads();
+  const int b = request_of_row(tab, row);
+  const ReqDev& rq = request(tab, b);
+  decide_row(rq, row, n, rs, a.dec);
+
+  // 3. the last row of the request to finish walks the request
+  __threadfence();
+  __syncthreads();
+  if (tid == 0)
+    last = atomicAdd(&a.req_ticket[b], 1u) == static_cast<uint32_t>(rq.n_nodes);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) a.req_ticket[b] = 0u;
+  accept_request(rq, a.vocab, a.dec, a.status, as);
+}
+
+__global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len, vr_policy pol,
+                              int32_t* __restrict__ out_m, float* __restrict__ out_e,
+                              float* __restrict__ out_S) {
+  __shared__ float vals[kPool];
+  __shared__ float e[kPool];
+  __shared__ int m;
+  __shared__ float S;
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x;
+  for (int j = threadIdx.x; j < kPool; j += 32) vals[j] = pool_vals[static_cast<size_t>(row) * kPool + j];
+  __syncwarp();
+  policy_warp(vals, pool_len, pol, e, &m, &S);
+  for (int j = threadIdx.x; j < kPool; j += 32) out_e[static_cast<size_t>(row) * kPool + j] = e[j];
+  if (threadIdx.x == 0) {
+    out_m[row] = m;
+    out_S[row] = S;
+  }
+}
+
+}  // namespace smp
+
+int select_segments(int vocab) {
+  int nseg = std::min((vocab + smp::SUB - 1) / smp::SUB, smp::MAX_SEG);
+  const long long per = (static_cast<long long>(vocab) + nseg - 1) / nseg;
+  const long long seg_len = (per + smp::SUB - 1) / smp::SUB * smp::SUB;
+  return static_cast<int>((vocab + seg_len - 1) / seg_len);
+}
+
+size_t select_cand_bytes(int rows, int vocab) {
+  return static_cast<size_t>(rows) * select_segments(vocab) * kPool * sizeof(uint64_t);
+}
+
+int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
+                  uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
+                  int4* dec, int32_t* status, cudaStream_t stream) {
+  const int nseg = select_segments(vocab);
+  const long long per = (static_cast<long long>(vocab) + nseg - 1) / nseg;
+  smp::SampleArgs a;
+  a.logits = logits;
+  a.vocab = vocab;
+  a.seg_len = static_cast<int>((per + smp::SUB - 1) / smp::SUB * smp::SUB);
+  a.nseg = nseg;
+  a.cand = cand;
+  a.row_ticket = row_ticket;
+  a.req_ticket = req_ticket;
+  a.pool_ids = pool_ids;
+  a.pool_vals = pool_vals;
+  a.dec = dec;
+  a.status = status;
+  a.decide = tab ? 1 : 0;
+  const size_t smem = sizeof(smp::StageShared);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(smp::sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return VR_ERR_CUDA;
+    attr_set = true;
+  }
+  ReqTable none{};
+  return launch_pdl(smp::sample_kernel, dim3(nseg, rows), dim3(smp::THREADS), smem, stream, a,
+                    tab ? *tab : none) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
+int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
+                  int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream) {
+  return launch_pdl(smp::policy_kernel, dim3(rows), dim3(32), 0, stream, pool_vals, pool_len, pol,
+                    out_m, out_e, out_S) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
+}  // namespace vr

@@ -11,12 +11,14 @@
 //
 // Rules of use (also stated in include/verifyrow.h):
 //   * rows <= VR_NOALLOC_SELECT_MAX_ROWS; any vocab (the select never splits a
-//     row into more than 80 segments of candidates);
+//     row into more than 64 segments of candidates);
 //   * the array is shared by every call on a device and keeps the last
 //     call's contents; calls that overlap on the GPU (two streams, or two
 //     host threads) race on it and must be serialised by the caller;
-//   * nothing in it needs to start at zero: the first phase of the select
-//     writes every candidate slot that the second phase reads;
+//   * the row counters that pick each row's merging CTA must start at zero;
+//     every call clears them (an asynchronous memset on the caller's stream)
+//     before its kernel; the candidate slots are written before they are
+//     read;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress with that device current) and remembers it, so
 //     make that first call before any stream capture on that device.
@@ -28,12 +30,14 @@
 namespace vr {
 namespace {
 
-constexpr int kNoallocMaxSegments = 80;
+constexpr int kNoallocMaxSegments = 64;
 constexpr size_t kNoallocSlots =
     static_cast<size_t>(VR_NOALLOC_SELECT_MAX_ROWS) * kNoallocMaxSegments * kPool;
+constexpr size_t kCounterSlots = 32;   // 256 bytes holding the 32 uint32 row counters
 
-// 32 rows x 80 segments x 64 candidates x 8 bytes = 1.25 MiB
-static __device__ __align__(256) uint64_t g_select_scratch[kNoallocSlots];
+// the row counters, then 32 rows x 64 segments x 64 candidates x 8 bytes:
+// 1 MiB + 256 B
+static __device__ __align__(256) uint64_t g_select_scratch[kCounterSlots + kNoallocSlots];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -64,6 +68,10 @@ extern "C" int vr_verify_select_noalloc(const float* logits, int rows, int vocab
     return VR_ERR_UNSUPPORTED;
   uint64_t* scratch = vr::scratch_for_current_device();
   if (!scratch) return VR_ERR_CUDA;
-  return vr::launch_select(logits, rows, vocab, scratch, pool_ids, pool_vals, nullptr, nullptr,
-                           static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(scratch);
+  if (cudaMemsetAsync(counters, 0, VR_NOALLOC_SELECT_MAX_ROWS * sizeof(uint32_t), s) != cudaSuccess)
+    return VR_ERR_CUDA;
+  return vr::launch_sample(logits, rows, vocab, scratch + vr::kCounterSlots, counters, nullptr,
+                           pool_ids, pool_vals, nullptr, nullptr, nullptr, s);
 }

@@ -9,6 +9,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/verifyrow.h"
@@ -230,6 +231,35 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
     *S_out = S;
   }
   __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch.  Every kernel of the library lets the next
+// kernel on the stream start launching at once (launch_dependents) and waits
+// for its predecessor grid to complete before it touches any buffer that a
+// predecessor may write or read (wait).  Since each kernel waits for the
+// previous one, completion still follows stream order; only launch latency
+// and prologues overlap.  Without the launch attribute both are no-ops.
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) {

@@ -21,19 +21,18 @@ int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int 
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab,
                     bool with_q, int32_t* status, cudaStream_t stream);
 
-// pool select: logits [rows][vocab] -> pool ids/vals [rows][64]; with a
-// request table also the policy and the per-row decisions
-// dec[row] = (argmax, emit draw y, residual draw z, accept bit)
+// sampling stage, one kernel: logits [rows][vocab] -> pool ids/vals
+// [rows][64]; with a request table also the policy, the per-row decisions
+// dec[row] = (argmax, emit draw y, residual draw z, accept bit) and the
+// acceptance walk of every request.  row_ticket [rows] and req_ticket
+// [requests] must be zero on entry and are zero again on exit.
 int select_segments(int vocab);
 size_t select_cand_bytes(int rows, int vocab);
-int launch_select(const float* logits, int rows, int vocab, uint64_t* cand, int32_t* pool_ids,
-                  float* pool_vals, const ReqTable* tab, int4* dec, cudaStream_t stream);
+int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
+                  uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
+                  int4* dec, int32_t* status, cudaStream_t stream);
 
 int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
                   int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream);
-
-// acceptance: one CTA per request
-int launch_accept(const ReqTable& tab, int n_req, int vocab, const int4* dec, int32_t* status,
-                  cudaStream_t stream);
 
 }  // namespace vr
