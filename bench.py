@@ -327,12 +327,19 @@ def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
     ws = vb.workspace(R, H5, V, device=dev)
 
     def batched(i):
-        vb.verify_window_batched(wd5, A, reqs, lg, ws, pen_logits=pen, stream=stream)
+        vb.verify_window_batched(wd5, A, reqs, lg, ws, pen_logits=pen, path=vb.VR_PATH_TC_BATCH,
+                                 stream=stream)
     t = _event_time(torch, stream, batched, max(5, n_steps // 50))
     flops = 2.0 * R * H5 * V
+    # the projection alone, for the tensor-pipe roofline (2 bf16 planes)
+    tp = _event_time(torch, stream,
+                     lambda i: vb.verify_project(wd5, A, lg, ws, path=vb.VR_PATH_TC_BATCH,
+                                                 stream=stream), max(5, n_steps // 50))
     out["batched_64x4_h5120"] = {"windows_per_s": nreq / t, "us_per_call": 1e6 * t, "rows": R,
-                                 "algorithmic_tflops": flops / t / 1e12,
-                                 "weight_gbs": V * H5 * 2 / t / 1e9}
+                                 "path": "tc_batch", "projection_us": 1e6 * tp,
+                                 "algorithmic_tflops": flops / tp / 1e12,
+                                 "executed_tflops": 2 * flops / tp / 1e12,
+                                 "weight_gbs": V * H5 * 2 / tp / 1e9}
     del wd5
     return out
 

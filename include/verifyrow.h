@@ -71,6 +71,7 @@ extern "C" {
 #define VR_PATH_AUTO 0           /* = VR_PATH_TC                               */
 #define VR_PATH_FFMA 1           /* CUDA-core multi-row GEMV (fp32 FMA)        */
 #define VR_PATH_TC 2             /* tcgen05 tensor cores, exact 3-plane split  */
+#define VR_PATH_TC_BATCH 3       /* tcgen05, rows as M in groups of 256, 2 planes */
 
 /* limits */
 #define VR_POOL 64               /* pool width ("Speculative decoding on RDNA" §03) */
@@ -133,10 +134,17 @@ VR_API int vr_workspace_bytes(int rows, int hidden, int vocab, size_t* out_bytes
  * weights are read once for all k + 1 rows; §02: multi-row projections sum
  * in the single-row order).
  *   logits[r][v] = sum_h weight[v][h] * act[r][h], fp32 accumulation.
- * Each weight byte is streamed from HBM once per call for all rows.  For a
- * given path, hidden and vocab, the bits of row r do not depend on `rows`
- * or on the other rows' values, so a row computed inside an R-row call is
- * identical to the same row computed alone.
+ * Paths (chosen per weight matrix, never by row count):
+ *   VR_PATH_TC (= AUTO): rows in groups of 32, activations split exactly into
+ *     three bf16 planes (exact products); the weights stream once per group.
+ *   VR_PATH_TC_BATCH: rows in groups of 256 as the MMA's M side, two bf16
+ *     planes (16 significant bits, error below 2^-17 |a|); weights stream once
+ *     per group.  For many rows (batched serving), where the tensor pipe sets
+ *     the pace.
+ *   VR_PATH_FFMA: CUDA-core FMAs, rows in passes of up to 8.
+ * For a given path, hidden and vocab, the bits of row r do not depend on
+ * `rows` or on the other rows' values, so a row computed inside an R-row
+ * call is identical to the same row computed alone.
  * rows in [1, VR_MAX_ROWS]; hidden a multiple of 8 in [8, 65536];
  * vocab in [1, 2^31 - 1].  path: VR_PATH_*.  Writes logits only.
  */

@@ -32,6 +32,7 @@ VR_DEV_TIMEOUT = 8
 VR_PATH_AUTO = 0
 VR_PATH_FFMA = 1
 VR_PATH_TC = 2
+VR_PATH_TC_BATCH = 3
 VR_POOL = 64
 VR_QCAND = 8
 VR_MAX_WINDOW_ROWS = 64

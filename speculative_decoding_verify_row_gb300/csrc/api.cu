@@ -1,5 +1,6 @@
 // C ABI of libverifyrow: argument validation, workspace layout and the
 // order of launches of each entry point.  See include/verifyrow.h.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -34,7 +35,7 @@ Layout layout(int rows, int hidden, int vocab) {
   };
   const size_t r = static_cast<size_t>(rows);
   L.status = take(kControlBytes);
-  L.planes = take(tc_plane_bytes(rows, hidden));
+  L.planes = take(std::max(tc_plane_bytes(rows, hidden), tcb_plane_bytes(rows, hidden)));
   L.cand = take(select_cand_bytes(rows, vocab));
   L.pool_ids = take(r * kPool * 4);
   L.pool_vals = take(r * kPool * 4);
@@ -138,6 +139,9 @@ int project(const uint16_t* weight, const float* act, int rows, int hidden, int 
   if (path == VR_PATH_TC)
     return launch_project_tc(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
                              at<int32_t>(ws, L.status), s);
+  if (path == VR_PATH_TC_BATCH)
+    return launch_project_tcb(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
+                              at<int32_t>(ws, L.status), s);
   if (path == VR_PATH_FFMA) return launch_project_ffma(weight, act, rows, hidden, vocab, logits, s);
   return VR_ERR_ARG;
 }
@@ -222,7 +226,7 @@ int vr_verify_project(const uint16_t* weight, const float* act, int rows, int hi
   int st = check_shape(rows, hidden, vocab);
   if (st != VR_OK) return st;
   if (!weight || !act || !logits) return VR_ERR_ARG;
-  if (path < VR_PATH_AUTO || path > VR_PATH_TC) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH) return VR_ERR_ARG;
   if (!aligned16(weight)) return VR_ERR_ARG;
   if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
   return project(weight, act, rows, hidden, vocab, path, logits, ws, layout(rows, hidden, vocab),
@@ -297,7 +301,7 @@ int vr_verify_window(const uint16_t* weight, const float* act, int rows, int hid
   if (st != VR_OK) return st;
   if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
   if (!weight || !act || !logits || !out_ids || !out_accept || !out_n_emitted) return VR_ERR_ARG;
-  if (path < VR_PATH_AUTO || path > VR_PATH_TC || !aligned16(weight)) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH || !aligned16(weight)) return VR_ERR_ARG;
   if ((st = check_window(rows, n_nodes, tokens, q_ids, q_logits, hist, hist_len)) != VR_OK) return st;
   if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
   return window_device(weight, act, rows, hidden, vocab, path, tokens, parent, n_nodes, q_ids,
@@ -311,7 +315,7 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
                              float* pen_logits, void* ws, size_t ws_bytes, void* stream) {
   if (!reqs || n_req < 1 || n_req > VR_MAX_REQUESTS) return VR_ERR_ARG;
   if (!weight || !act || !logits || !aligned16(weight)) return VR_ERR_ARG;
-  if (path < VR_PATH_AUTO || path > VR_PATH_TC) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH) return VR_ERR_ARG;
   int rows = 0, st;
   bool any_active = false, any_q = false;
   for (int b = 0; b < n_req; ++b) {
@@ -378,7 +382,7 @@ int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, 
   if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
   if (!weight || !act_h || !logits || !out_ids_h || !out_accept_h || !out_n_emitted_h)
     return VR_ERR_ARG;
-  if (path < VR_PATH_AUTO || path > VR_PATH_TC || !aligned16(weight)) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH || !aligned16(weight)) return VR_ERR_ARG;
   if ((st = check_window(rows, n_nodes, tokens_h, q_ids_h, q_logits_h, hist_h, hist_len)) != VR_OK)
     return st;
   if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;

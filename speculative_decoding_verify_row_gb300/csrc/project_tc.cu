@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include "tc_common.cuh"
 #include "vr_common.cuh"
 #include "vr_kernels.h"
 
@@ -55,120 +56,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
-constexpr long long kWaitLimitCycles = 4000000000ll;  // ~2 s at 2 GHz
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait.  Returns false (and raises the CTA's abort flag and the
-// device status) if the phase does not complete in time, or if another role
-// of the CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      *abort_flag = 1;
-      set_status(status, VR_DEV_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-// L2 policies: the weights are streamed once per window and must not push
-// anything else out of L2 (the logits the next kernel reads, the planes every
-// CTA re-reads, the code and scratch of the sampling stage), so they are
-// loaded evict-first; the plane tiles, shared by all CTAs, evict-last.
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core
-// groups 1024 B apart (SBO), descriptor version 1 (bit 46), swizzle mode 2
-// (bits 61-63).  The leading offset is unused for this layout.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(16 >> 4) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+using namespace tcx;
 
 __global__ void __launch_bounds__(THREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
@@ -293,7 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int ks = 0; ks < BK / 16; ++ks) {
               // advance 16 bf16 = 32 bytes along K inside the swizzled row
-              mma_bf16(dcol + mt * BN, adesc + 2 * ks, bdesc + 2 * ks, (kb | ks) ? 1u : 0u);
+              mma_bf16_desc(dcol + mt * BN, adesc + 2 * ks, bdesc + 2 * ks, kIdesc,
+                            (kb | ks) ? 1u : 0u);
             }
           }
           mma_commit(empty_bar(s));
@@ -421,8 +310,15 @@ bool get_encoder() {
   return true;
 }
 
-bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                    uint32_t box_inner, uint32_t box_outer) {
+int g_num_sms = 0;
+bool g_attr_set = false;
+}  // namespace
+
+// 2-D bf16 tensor map over a row-major [outer][inner] array, tiles of
+// box_outer x box_inner elements, 128-byte swizzle (box_inner * 2 == 128).
+bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer) {
+  if (!get_encoder()) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -433,10 +329,6 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_num_sms = 0;
-bool g_attr_set = false;
-}  // namespace
-
 size_t tc_plane_bytes(int rows, int hidden) {
   const int groups = (rows + tc::NP - 1) / tc::NP;
   return static_cast<size_t>(groups) * tc::BN * hidden * 2;
@@ -444,7 +336,6 @@ size_t tc_plane_bytes(int rows, int hidden) {
 
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, void* planes, int32_t* status, cudaStream_t stream) {
-  if (!get_encoder()) return VR_ERR_CUDA;
   if (!g_num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return VR_ERR_CUDA;
@@ -469,14 +360,14 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
       return VR_ERR_CUDA;
   }
   CUtensorMap tm_w;
-  if (!encode_bf16_2d(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
+  if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
   const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
   const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
   const int grid = std::min(n_units, g_num_sms);
   for (int g = 0; g < groups; ++g) {
     CUtensorMap tm_b;
-    if (!encode_bf16_2d(&tm_b, pl + static_cast<size_t>(g) * tc::BN * hidden, hidden, tc::BN,
-                        tc::BK, tc::BN))
+    if (!encode_bf16_tile(&tm_b, pl + static_cast<size_t>(g) * tc::BN * hidden, hidden, tc::BN,
+                          tc::BK, tc::BN))
       return VR_ERR_ARG;
     const int rg = std::min(tc::NP, rows - g * tc::NP);
     if (launch_pdl(tc::project_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "vr_common.cuh"
@@ -10,7 +11,12 @@
 namespace vr {
 
 // projection
+bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer);
 size_t tc_plane_bytes(int rows, int hidden);
+size_t tcb_plane_bytes(int rows, int hidden);
+int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
+                       float* logits, void* planes, int32_t* status, cudaStream_t stream);
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, void* planes, int32_t* status, cudaStream_t stream);
 int ffma_rows_per_pass(int hidden);

@@ -10,7 +10,7 @@ from speculative_decoding_verify_row_gb300 import binding as vb, synth
 from gpu_common import require_gpu, dev_weight, dev, project, assert_logits_close
 
 pytestmark = pytest.mark.gpu
-PATHS = [vb.VR_PATH_TC, vb.VR_PATH_FFMA]
+PATHS = [vb.VR_PATH_TC, vb.VR_PATH_FFMA, vb.VR_PATH_TC_BATCH]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -77,3 +77,20 @@ def test_full_size_sampled_rows(big_weight, path):
                         ov.project_columns(W, A, cols))
     one = project(Wd, A[7:8], path)
     assert torch.equal(one[0].view(torch.int32), got[7].view(torch.int32))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_row_bits_across_row_groups(path):
+    """More rows than one group of any path (300 > 256 > 32 > 8): every row
+    equals the same row computed alone, and matches the oracle."""
+    rng = np.random.default_rng(12)
+    V, H = 1100, 520
+    Wb = synth.f32_to_bf16_bits(rng.standard_normal((V, H), dtype=np.float32) * np.float32(0.03))
+    W = dev_weight(Wb)
+    A = rng.standard_normal((300, H), dtype=np.float32)
+    full = project(W, A, path)
+    assert_logits_close(full.cpu().numpy(), ov.project(Wb, A))
+    full = full.cpu().numpy().view(np.uint32)
+    for r in (0, 31, 32, 255, 256, 299):
+        alone = project(W, A[r:r + 1], path).cpu().numpy().view(np.uint32)
+        assert np.array_equal(alone[0], full[r]), r

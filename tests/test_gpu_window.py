@@ -213,7 +213,8 @@ def test_token_tree_full_size(big_weights_4096, temperature):
     assert stats["compared"] >= 2
 
 
-def test_batched_serving(big_weights_5120):
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+def test_batched_serving(big_weights_5120, path):
     """64 requests x k 3 (256 rows), hidden 5120; even requests greedy, odd
     ones T 0.8 / top-k 20 / top-p 0.9 / presence 1.5; 2048-token Zipf
     histories, W 64, seeds 0..63.  Checked on 8 requests against the
@@ -255,7 +256,7 @@ def test_batched_serving(big_weights_5120):
     logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
     pen = torch.empty_like(logits)
     ws = vb.workspace(R, H, V)
-    vb.verify_window_batched(bw.dev, dev(A), reqs, logits, ws, pen_logits=pen)
+    vb.verify_window_batched(bw.dev, dev(A), reqs, logits, ws, pen_logits=pen, path=path)
     torch.cuda.synchronize()
     assert vb.device_status(ws) == 0
     stats = {}
