@@ -21,7 +21,7 @@ constexpr size_t kControlBytes = 8192;
 static_assert(kReqTicketOff + VR_MAX_REQUESTS * 4 <= kControlBytes, "control region");
 
 struct Layout {
-  size_t status, planes, cand, pool_ids, pool_vals, dec, q_pen, reqs, row_req;
+  size_t status, planes, cand, gmax, pool_ids, pool_vals, dec, q_pen, reqs, row_req;
   size_t st_act, st_tok, st_par, st_qid, st_qlog, st_hist, st_out, total;
 };
 
@@ -37,6 +37,7 @@ Layout layout(int rows, int hidden, int vocab) {
   L.status = take(kControlBytes);
   L.planes = take(std::max(tc_plane_bytes(rows, hidden), tcb_plane_bytes(rows, hidden)));
   L.cand = take(select_cand_bytes(rows, vocab));
+  L.gmax = take(r * ((static_cast<size_t>(vocab) + 31) / 32) * 4);
   L.pool_ids = take(r * kPool * 4);
   L.pool_vals = take(r * kPool * 4);
   L.dec = take(r * sizeof(int4));
@@ -133,28 +134,41 @@ ReqTable single(const ReqDev& r) {
 }
 
 
+// gmax (nullable): where the tensor-core paths also record the group maxima
 int project(const uint16_t* weight, const float* act, int rows, int hidden, int vocab, int path,
-            float* logits, void* ws, const Layout& L, cudaStream_t s) {
+            float* logits, uint32_t* gmax, void* ws, const Layout& L, cudaStream_t s) {
   if (path == VR_PATH_AUTO) path = VR_PATH_TC;
   if (path == VR_PATH_TC)
     return launch_project_tc(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
-                             at<int32_t>(ws, L.status), s);
+                             gmax, at<int32_t>(ws, L.status), s);
   if (path == VR_PATH_TC_BATCH)
     return launch_project_tcb(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
-                              at<int32_t>(ws, L.status), s);
+                              gmax, at<int32_t>(ws, L.status), s);
   if (path == VR_PATH_FFMA) return launch_project_ffma(weight, act, rows, hidden, vocab, logits, s);
   return VR_ERR_ARG;
 }
 
-// penalties -> pool + policy -> acceptance, for requests already in `tab`
+// True when the projection path records group maxima for the sampling stage
+bool records_gmax(int path, int vocab) {
+  return (path == VR_PATH_AUTO || path == VR_PATH_TC || path == VR_PATH_TC_BATCH) &&
+         sample_rows_supported(vocab);
+}
+
+// penalties -> pool + policy -> acceptance, for requests already in `tab`;
+// gmax: the group maxima of `target` if the projection recorded them
 int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* target,
-                  bool any_active, bool any_q, void* ws, const Layout& L, cudaStream_t s) {
+                  uint32_t* gmax, bool any_active, bool any_q, void* ws, const Layout& L,
+                  cudaStream_t s) {
   int st;
   if (any_active) {
-    st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);
+    st = launch_penalize(tab, rows, target, vocab, any_q, gmax, at<int32_t>(ws, L.status), s);
     if (st != VR_OK) return st;
   }
   (void)n_req;
+  if (gmax)
+    return launch_sample_rows(target, rows, vocab, gmax, at<uint32_t>(ws, L.status + kReqTicketOff),
+                              at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
+                              at<int4>(ws, L.dec), at<int32_t>(ws, L.status), s);
   return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
                        at<uint32_t>(ws, L.status + kReqTicketOff), at<int32_t>(ws, L.pool_ids),
@@ -168,7 +182,8 @@ int window_device(const uint16_t* weight, const float* act, int rows, int hidden
                   const vr_policy& pol, uint64_t seed, uint64_t position, float* logits,
                   float* pen_logits, int32_t* out_ids, int32_t* out_accept, int32_t* out_n,
                   void* ws, const Layout& L, cudaStream_t s) {
-  int st = project(weight, act, rows, hidden, vocab, path, logits, ws, L, s);
+  uint32_t* gmax = records_gmax(path, vocab) ? at<uint32_t>(ws, L.gmax) : nullptr;
+  int st = project(weight, act, rows, hidden, vocab, path, logits, gmax, ws, L, s);
   if (st != VR_OK) return st;
   const bool act_pen = active(pol);
   float* target = logits;
@@ -181,7 +196,7 @@ int window_device(const uint16_t* weight, const float* act, int rows, int hidden
   float* q_pen = (act_pen && q_ids) ? at<float>(ws, L.q_pen) : const_cast<float*>(q_logits);
   const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_pen, hist,
                                        hist_len, pol, seed, position, out_ids, out_accept, out_n));
-  return sample_stages(tab, 1, rows, vocab, target, act_pen, q_ids != nullptr, ws, L, s);
+  return sample_stages(tab, 1, rows, vocab, target, gmax, act_pen, q_ids != nullptr, ws, L, s);
 }
 
 }  // namespace
@@ -229,8 +244,8 @@ int vr_verify_project(const uint16_t* weight, const float* act, int rows, int hi
   if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH) return VR_ERR_ARG;
   if (!aligned16(weight)) return VR_ERR_ARG;
   if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
-  return project(weight, act, rows, hidden, vocab, path, logits, ws, layout(rows, hidden, vocab),
-                 static_cast<cudaStream_t>(stream));
+  return project(weight, act, rows, hidden, vocab, path, logits, nullptr, ws,
+                 layout(rows, hidden, vocab), static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_penalize(float* logits, int rows, int vocab, const int32_t* tokens,
@@ -246,8 +261,8 @@ int vr_verify_penalize(float* logits, int rows, int vocab, const int32_t* tokens
   const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_logits, hist,
                                        hist_len, *policy, 0, 0, nullptr, nullptr, nullptr));
   const Layout L = layout(rows, 8, vocab);
-  return launch_penalize(tab, rows, logits, vocab, q_ids != nullptr, at<int32_t>(ws, L.status),
-                         static_cast<cudaStream_t>(stream));
+  return launch_penalize(tab, rows, logits, vocab, q_ids != nullptr, nullptr,
+                         at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids,
@@ -287,8 +302,8 @@ int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab, const 
   const ReqTable tab =
       single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, const_cast<float*>(q_logits),
                       nullptr, 0, *policy, seed, position, out_ids, out_accept, out_n_emitted));
-  return sample_stages(tab, 1, rows, vocab, const_cast<float*>(pen_logits), false, false, ws, L,
-                       static_cast<cudaStream_t>(stream));
+  return sample_stages(tab, 1, rows, vocab, const_cast<float*>(pen_logits), nullptr, false, false,
+                       ws, L, static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_window(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
@@ -354,7 +369,8 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return VR_ERR_CUDA;
 
-  st = project(weight, act, rows, hidden, vocab, path, logits, ws, L, s);
+  uint32_t* gmax = records_gmax(path, vocab) ? at<uint32_t>(ws, L.gmax) : nullptr;
+  st = project(weight, act, rows, hidden, vocab, path, logits, gmax, ws, L, s);
   if (st != VR_OK) return st;
   float* target = logits;
   if (any_active && pen_logits) {
@@ -367,7 +383,7 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
   tab.many = at<ReqDev>(ws, L.reqs);
   tab.row_req = at<int32_t>(ws, L.row_req);
   tab.n_req = n_req;
-  return sample_stages(tab, n_req, rows, vocab, target, any_active, any_q, ws, L, s);
+  return sample_stages(tab, n_req, rows, vocab, target, gmax, any_active, any_q, ws, L, s);
 }
 
 int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,

@@ -22,7 +22,7 @@ constexpr int THREADS = 128;
 
 __global__ void __launch_bounds__(THREADS)
     penalize_kernel(ReqTable tab, int rows_total, float* __restrict__ logits, int vocab,
-                    int with_q, int32_t* status) {
+                    int with_q, uint32_t* __restrict__ gmax, int32_t* status) {
   __shared__ int32_t H[VR_MAX_PENALTY_WINDOW];
   __shared__ int32_t path[VR_MAX_WINDOW_ROWS];
   __shared__ int h_len, bad;
@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(THREADS)
   pdl_trigger();
   pdl_wait();
   const bool is_q = blockIdx.x >= static_cast<unsigned>(rows_total);
-  const int g = is_q ? blockIdx.x - rows_total : blockIdx.x;   // global row
+  const int g_row = is_q ? blockIdx.x - rows_total : blockIdx.x;   // global row
+  const int g = g_row;
   const ReqDev& rq = request(tab, request_of_row(tab, g));
   const vr_policy& pol = rq.pol;
   const int local = g - rq.row0;
@@ -93,6 +94,26 @@ __global__ void __launch_bounds__(THREADS)
       }
       if (first && t >= 0 && t < vocab) row[t] = penalize_value(row[t], count, pol);
     }
+    if (gmax) {
+      // refresh the largest order key of every 32-row group a penalty touched
+      __syncthreads();
+      const int ngroups = (vocab + 31) / 32;
+      for (int j = threadIdx.x; j < len; j += THREADS) {
+        const int t = H[j];
+        if (t < 0 || t >= vocab) continue;
+        const int g = t >> 5;
+        bool first = true;
+        for (int i = 0; i < j; ++i)
+          if (H[i] >= 0 && H[i] < vocab && (H[i] >> 5) == g) first = false;
+        if (!first) continue;
+        uint32_t k = 0u;
+        for (int v = g * 32; v < g * 32 + 32 && v < vocab; ++v) {
+          const uint32_t kv = float_key(row[v]);
+          k = kv > k ? kv : k;
+        }
+        gmax[static_cast<size_t>(g_row) * ngroups + g] = k;
+      }
+    }
   } else {
     // candidates of node `local`, written to the request's q buffer
     const int32_t* ids = rq.q_ids + static_cast<size_t>(local) * kQCand;
@@ -125,13 +146,13 @@ __global__ void copy_q_kernel(ReqTable tab, int rows_total) {
 }  // namespace pen
 
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab, bool with_q,
-                    int32_t* status, cudaStream_t stream) {
+                    uint32_t* gmax, int32_t* status, cudaStream_t stream) {
   if (with_q && launch_pdl(pen::copy_q_kernel, dim3(rows_total), dim3(32), 0, stream, tab,
                           rows_total) != cudaSuccess)
     return VR_ERR_CUDA;
   const int blocks = rows_total * (with_q ? 2 : 1);
   return launch_pdl(pen::penalize_kernel, dim3(blocks), dim3(pen::THREADS), 0, stream, tab,
-                    rows_total, logits, vocab, with_q ? 1 : 0, status) == cudaSuccess
+                    rows_total, logits, vocab, with_q ? 1 : 0, gmax, status) == cudaSuccess
              ? VR_OK
              : VR_ERR_CUDA;
 }

@@ -20,6 +20,9 @@
 //    warp 1 issues the MMAs into a double-buffered TMEM accumulator
 //    (2 x 192 columns); warps 2-5 drain TMEM and write the logits, so the
 //    epilogue of one unit overlaps the weight stream of the next.
+//  * Optionally the epilogue also records, per row and per 32 vocabulary
+//    rows, the largest order key (a warp max), which lets the sampling stage
+//    find a row's top 64 without reading the whole row.
 //  * All mbarrier waits are bounded: on time-out the CTA records
 //    VR_DEV_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <algorithm>
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b, int hidden, int vocab,
                       int rows_in_group, int row_base, float* __restrict__ logits,
-                      int32_t* status) {
+                      uint32_t* __restrict__ gmax, int ngroups, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -218,20 +221,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t dcol = tmem_base + lane_off + buf * TMEM_COLS_PER_BUF;
       for (int mt = 0; mt < nmt; ++mt) {
-        const int v = (u * MT + mt) * BM + quarter * 32 + lane;
+        const int vbase = (u * MT + mt) * BM + quarter * 32;     // this warp's 32 vocab rows
+        const int v = vbase + lane;
         for (int rb = 0; rb < rows_in_group; rb += 8) {
           float hi[8], mid[8], lo[8];
           tmem_ld8(dcol + mt * BN + 0 * NP + rb, hi);
           tmem_ld8(dcol + mt * BN + 1 * NP + rb, mid);
           tmem_ld8(dcol + mt * BN + 2 * NP + rb, lo);
           tmem_ld_wait();
-          if (v < vocab) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = rb + i;
-              if (r < rows_in_group)
-                logits[static_cast<size_t>(row_base + r) * vocab + v] =
-                    __fadd_rn(__fadd_rn(hi[i], mid[i]), lo[i]);
+          for (int i = 0; i < 8; ++i) {
+            const int r = rb + i;
+            if (r < rows_in_group) {
+              const float x = __fadd_rn(__fadd_rn(hi[i], mid[i]), lo[i]);
+              if (v < vocab) logits[static_cast<size_t>(row_base + r) * vocab + v] = x;
+              if (gmax && vbase < vocab) {
+                // the largest order key of these 32 vocabulary rows
+                const uint32_t k =
+                    __reduce_max_sync(0xffffffffu, v < vocab ? float_key(x) : 0u);
+                if (lane == 0) gmax[static_cast<size_t>(row_base + r) * ngroups + (vbase >> 5)] = k;
+              }
             }
           }
         }
@@ -335,7 +344,8 @@ size_t tc_plane_bytes(int rows, int hidden) {
 }
 
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                      float* logits, void* planes, int32_t* status, cudaStream_t stream) {
+                      float* logits, void* planes, uint32_t* gmax, int32_t* status,
+                      cudaStream_t stream) {
   if (!g_num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return VR_ERR_CUDA;
@@ -371,7 +381,8 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
       return VR_ERR_ARG;
     const int rg = std::min(tc::NP, rows - g * tc::NP);
     if (launch_pdl(tc::project_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
-                   tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, status) != cudaSuccess)
+                   tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, gmax,
+                   (vocab + 31) / 32, status) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;

@@ -21,6 +21,8 @@
 //  * Warp 0 feeds a 2-stage TMA ring (32 KB of weights, evict-first in L2,
 //    and 64 KB of plane tiles, evict-last, per stage), one thread of warp 1
 //    issues M128 N256 K16 MMAs, warps 2-5 drain TMEM into the logits.
+//  * Optionally the epilogue records, per row and per 32 vocabulary rows, the
+//    largest order key (the sampling stage's filter).
 //  * All waits are bounded (VR_DEV_TIMEOUT), as in the chain projection.
 #include <algorithm>
 
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     project_tcb_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_a, int hidden, int vocab,
                        int rows_in_group, int row_base, float* __restrict__ logits,
-                       int vec_ok, int32_t* status) {
+                       int vec_ok, uint32_t* __restrict__ gmax, int ngroups, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -208,6 +210,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tmem_base + lane_off + mh * BN + c * 32, v);
           tmem_ld_wait();
           const int v0 = t * BN + c * 32;
+          if (gmax && rl < rows_in_group && v0 < vocab) {
+            // the largest order key of these 32 vocabulary rows of this row
+            uint32_t k = 0u;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t ki = (v0 + i < vocab) ? float_key(v[i]) : 0u;
+              k = ki > k ? ki : k;
+            }
+            gmax[static_cast<size_t>(row_base + rl) * ngroups + (v0 >> 5)] = k;
+          }
           if (rl < rows_in_group) {
             if (vec && v0 + 32 <= vocab) {
 #pragma unroll
@@ -279,7 +291,8 @@ size_t tcb_plane_bytes(int rows, int hidden) {
 }
 
 int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                       float* logits, void* planes, int32_t* status, cudaStream_t stream) {
+                       float* logits, void* planes, uint32_t* gmax, int32_t* status,
+                       cudaStream_t stream) {
   if (!g_tcb_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -316,7 +329,7 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
     const int rg = std::min(tcb::GROUP, rows - g * tcb::GROUP);
     if (launch_pdl(tcb::project_tcb_kernel, dim3(grid), dim3(tcb::THREADS), tcb::SMEM_BYTES,
                    stream, tm_w, tm_a, hidden, vocab, rg, g * tcb::GROUP, logits, vec_ok,
-                   status) != cudaSuccess)
+                   gmax, (vocab + 31) / 32, status) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return VR_OK;

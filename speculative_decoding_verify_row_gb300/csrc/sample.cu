@@ -9,8 +9,10 @@
 // set is unique.
 //
 // Grid (segments, rows), no CTA ever waits for another:
-//  1. every CTA reduces its segment of one row to the segment's top 64 by a
-//     block radix select and stores them in pool order;
+//  1. every CTA reduces its segment of one row to the segment's top 64 (a
+//     threshold filter from per-thread maxima plus rank counting; a block
+//     radix select when ties defeat the filter) and stores them in pool
+//     order;
 //  2. it takes a ticket on the row's counter; the CTA that draws the last
 //     ticket has every segment list of the row available, merges them
 //     pairwise (merge path) into the row's pool, applies the sampler policy
@@ -45,13 +47,20 @@ struct SelectShared {
   uint32_t hist[MAX_BINS];
   uint64_t gather[GATHER_MAX];
   uint64_t out[kPool];
+  uint64_t sorted[kPool];
+  uint64_t warp_thr[THREADS / 32];
   uint32_t warp_sum[THREADS / 32];
   int count, gcount, digit, above, n_valid;
 };
 
+constexpr int MERGE_GATHER = 512;
+
 struct MergeShared {
   uint64_t in[MAX_SEG][kPool];
   uint64_t out[MAX_SEG / 2][kPool];
+  uint64_t gather[MERGE_GATHER];
+  uint64_t thr;
+  int count;
 };
 
 union StageShared {
@@ -59,13 +68,29 @@ union StageShared {
   MergeShared mrg;
 };
 
+constexpr int GI_MAX = 20;          // group maxima per thread: vocab <= 32 * 256 * 20
+constexpr int C_MAX = kPool * 32;   // candidates of the chosen groups, at most
+
+struct RowsShared {
+  SelectShared sel;
+  uint64_t cands[C_MAX];
+  uint64_t pool[kPool];
+  int ccount;
+};
+
 struct RowShared {
-  float e[kPool], pc[kPool], r[kPool], pr[kPool];
-  float qe[kPool], qp[kQCand];
+  __align__(16) float e[kPool];
+  __align__(16) float pc[kPool];
+  __align__(16) float r[kPool];
+  __align__(16) float pr[kPool];
+  __align__(16) float qe[kPool];
+  __align__(16) float qpc[kPool];
+  float qp[kQCand];
   float vals[kPool], qv[kQCand];
   int32_t ids[kPool], qid[kQCand];
   int m, qm, chain, acc;
-  float S, qS;
+  int32_t draft;
+  float S, qS, u1, u2;
 };
 
 struct AcceptShared {
@@ -120,11 +145,12 @@ __device__ __forceinline__ void find_digit(int nb, int need, SelectShared& sh) {
 // spread over many bins); once the entries that tie with the resolved prefix
 // are few (<= 256) they are gathered and the rest is decided by rank
 // counting; if they are exactly the ones still needed, all are taken.
-__device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
+template <int N>
+__device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31;
   int mine = 0;
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) mine += (x[i] != 0ull);
+  for (int i = 0; i < N; ++i) mine += (x[i] != 0ull);
   if (tid == 0) {
     sh.n_valid = 0;
     sh.count = 0;
@@ -147,7 +173,7 @@ __device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
       for (int b = tid; b < nb; b += THREADS) sh.hist[b] = 0u;
       __syncthreads();
 #pragma unroll
-      for (int i = 0; i < ITEMS; ++i)
+      for (int i = 0; i < N; ++i)
         if (x[i] != 0ull && (x[i] & mask) == prefix)
           atomicAdd(&sh.hist[static_cast<uint32_t>(x[i] >> shift) & (nb - 1)], 1u);
       __syncthreads();
@@ -161,7 +187,7 @@ __device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
       if (tie == need) break;                 // every tying entry is taken
       if (tie <= GATHER_MAX) {
 #pragma unroll
-        for (int i = 0; i < ITEMS; ++i)
+        for (int i = 0; i < N; ++i)
           if (x[i] != 0ull && (x[i] & mask) == prefix) sh.gather[atomicAdd(&sh.gcount, 1)] = x[i];
         __syncthreads();
         gathered = true;
@@ -171,11 +197,11 @@ __device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
   }
   if (!gathered) {
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i)
+    for (int i = 0; i < N; ++i)
       if (x[i] != 0ull && (x[i] & mask) >= prefix) sh.out[atomicAdd(&sh.count, 1)] = x[i];
   } else {
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i)
+    for (int i = 0; i < N; ++i)
       if (x[i] != 0ull && (x[i] & mask) > prefix) sh.out[atomicAdd(&sh.count, 1)] = x[i];
     const int g = sh.gcount;
     if (tid < g) {
@@ -186,6 +212,68 @@ __device__ void block_top64(const uint64_t (&x)[ITEMS], SelectShared& sh) {
     }
   }
   __syncthreads();
+}
+
+// Descending bitonic sort of one value per lane across a warp.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  return v;
+}
+
+// Top-64 of the block's nonzero composites, in pool order, into sh.sorted
+// (zero-padded).  Filter first: with t_w the 8th largest of the 32 per-thread
+// maxima of warp w, at least 8 entries of every warp reach min_w t_w, so at
+// least 64 entries of the block do (or all of them, if fewer exist).  The
+// entries at or above that threshold are compacted and ranked against each
+// other; rank < 64 is the pool position.  Returns false (nothing written)
+// when more than 256 entries pass, e.g. for rows full of ties; the caller
+// then falls back to the radix select.
+template <int N>
+__device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t mx = 0ull;
+#pragma unroll
+  for (int i = 0; i < N; ++i) mx = x[i] > mx ? x[i] : mx;
+  const uint64_t sorted = warp_sort_desc(mx);
+  if (lane == 7) sh.warp_thr[warp] = sorted;
+  if (tid == 0) sh.gcount = 0;
+  __syncthreads();
+  uint64_t thr = sh.warp_thr[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) thr = sh.warp_thr[w] < thr ? sh.warp_thr[w] : thr;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const bool pass = x[i] != 0ull && x[i] >= thr;
+    const uint32_t ball = __ballot_sync(0xffffffffu, pass);
+    if (ball) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sh.gcount, __popc(ball));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int pos = base + __popc(ball & ((1u << lane) - 1u));
+      if (pass && pos < GATHER_MAX) sh.gather[pos] = x[i];
+    }
+  }
+  __syncthreads();
+  const int n = sh.gcount;
+  if (n > GATHER_MAX) return false;
+  if (tid < kPool) sh.sorted[tid] = 0ull;
+  __syncthreads();
+  if (tid < n) {
+    const uint64_t me = sh.gather[tid];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += (sh.gather[j] > me);
+    if (rank < kPool) sh.sorted[rank] = me;
+  }
+  __syncthreads();
+  return true;
 }
 
 __device__ __forceinline__ uint64_t composite_at(const float* row, long long e) {
@@ -210,13 +298,61 @@ __device__ __forceinline__ uint64_t merged_at(const uint64_t* a, const uint64_t*
 }
 
 // Merge the row's nseg sorted lists (each the top 64 of its segment) into
-// the row's top 64: the top 64 of the union of two lists is the top 64 of
-// their merge, so merging pairs until one list is left gives the pool.
-// Returns the final list (shared memory).
+// the row's top 64, in pool order.  Returns the list (shared memory).
+//
+// Filter first: with tau the 8th largest of the lists' 8th entries, eight
+// lists hold eight entries each at or above tau, so the top 64 all lie at
+// or above it.  Those entries (usually about a hundred) are compacted and
+// ranked against each other.  If too many pass, the lists are merged
+// pairwise instead (merge path): the top 64 of the union of two lists is the
+// top 64 of their merge, so merging pairs until one list is left gives the
+// pool.
 __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeShared& ms) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < nseg * kPool; i += THREADS) ms.in[i / kPool][i % kPool] = lists[i];
+  if (tid == 0) ms.count = 0;
   __syncthreads();
+  if (nseg == 1) return ms.in[0];
+  if (tid < nseg) {
+    const uint64_t me = ms.in[tid][7];
+    int rank = 0;
+    for (int s = 0; s < nseg; ++s) {
+      const uint64_t o = ms.in[s][7];
+      rank += (o > me) || (o == me && s < tid);
+    }
+    if (rank == 7) ms.thr = me;
+  }
+  if (nseg < 8 && tid == 0) ms.thr = 1ull;       // fewer than 8 lists: take every entry
+  __syncthreads();
+  const uint64_t thr = ms.thr;
+  for (int base = 0; base < nseg * kPool; base += THREADS) {
+    const int i = base + tid;
+    const uint64_t v = i < nseg * kPool ? ms.in[i / kPool][i % kPool] : 0ull;
+    const bool pass = v != 0ull && v >= thr;
+    const uint32_t ball = __ballot_sync(0xffffffffu, pass);
+    if (ball) {
+      int at = 0;
+      if (lane == 0) at = atomicAdd(&ms.count, __popc(ball));
+      at = __shfl_sync(0xffffffffu, at, 0);
+      const int pos = at + __popc(ball & ((1u << lane) - 1u));
+      if (pass && pos < MERGE_GATHER) ms.gather[pos] = v;
+    }
+  }
+  __syncthreads();
+  const int n = ms.count;
+  if (n <= MERGE_GATHER) {
+    uint64_t* out = ms.out[0];
+    if (tid < kPool) out[tid] = 0ull;
+    __syncthreads();
+    for (int t = tid; t < n; t += THREADS) {
+      const uint64_t me = ms.gather[t];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += (ms.gather[j] > me);
+      if (rank < kPool) out[rank] = me;
+    }
+    __syncthreads();
+    return out;
+  }
   uint64_t(*src)[kPool] = ms.in;
   uint64_t(*dst)[kPool] = ms.out;
   int nl = nseg;
@@ -240,15 +376,6 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
 // ---------------------------------------------------------------------------
 // per-row decisions
 
-__device__ __forceinline__ int first_above(const float* c, int m, float t) {
-  // smallest j < m with c[j] > t, c non-decreasing; -1 if none
-  const int lane = threadIdx.x & 31;
-  uint32_t b = __ballot_sync(0xffffffffu, lane < m && c[lane] > t);
-  if (b) return __ffs(b) - 1;
-  b = __ballot_sync(0xffffffffu, lane + 32 < m && c[lane + 32] > t);
-  return b ? 32 + __ffs(b) - 1 : -1;
-}
-
 __device__ __forceinline__ int last_positive(const float* w, int m) {
   const int lane = threadIdx.x & 31;
   uint32_t b = __ballot_sync(0xffffffffu, lane + 32 < m && w[lane + 32] > 0.0f);
@@ -265,6 +392,8 @@ __device__ __forceinline__ int last_positive(const float* w, int m) {
 //      (p - q)+ renormalised with the same uniform (y if that is all zero);
 //   acc: u(row, accept) * q(x) < p(x) for the row's draft x (q(x) = 0:
 //      p(x) > 0).
+// Warp 0 applies the policy to the pool while warp 1 builds q, warp 2 draws
+// the row's two uniforms and warp 3 reads the draft token.
 __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4* dec) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const vr_policy& pol = rq.pol;
@@ -283,14 +412,7 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
   const uint64_t urow = static_cast<uint64_t>(local);
 
   if (warp == 0) {
-    policy_warp(rs.vals, n, pol, rs.e, &rs.m, &rs.S);
-    if (lane == 0) {
-      float acc = 0.0f;
-      for (int j = 0; j < rs.m; ++j) {
-        acc = __fadd_rn(acc, rs.e[j]);
-        rs.pc[j] = acc;
-      }
-    }
+    policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
   } else if (warp == 1 && reject_row) {
     // q: the node's candidates in pool order, then the same policy
     const float* qv = rq.q_pen + static_cast<size_t>(local) * kQCand;
@@ -308,32 +430,43 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
       rs.qv[rank] = qv[lane];
     }
     __syncwarp();
-    policy_warp(rs.qv, kQCand, pol, rs.qe, &rs.qm, &rs.qS);
+    policy_warp(rs.qv, kQCand, pol, rs.qe, rs.qpc, &rs.qm, &rs.qS);
     if (lane < rs.qm) rs.qp[lane] = __fdiv_rn(rs.qe[lane], rs.qS);
+  } else if (warp == 2) {
+    if (lane == 0) rs.u2 = uniform01(rq.seed, rq.position, urow, kPurposeEmit);
+    if (lane == 1 && reject_row) rs.u1 = uniform01(rq.seed, rq.position, urow, kPurposeAccept);
+  } else if (warp == 3 && lane == 0 && reject_row) {
+    rs.draft = rq.tokens[local];
   }
   __syncthreads();
   if (warp != 0) return;
 
   const int m = rs.m;
   const float S = rs.S;
-  const float u2 = uniform01(rq.seed, rq.position, urow, kPurposeEmit);
-  int j = first_above(rs.pc, m, __fmul_rn(u2, S));
+  const float u2 = rs.u2;
+  const float t2 = __fmul_rn(u2, S);
+  int j = warp_first(m, [&](int i) { return rs.pc[i] > t2; });
   if (j < 0) j = last_positive(rs.e, m);
   const int32_t y = rs.ids[j];
   int32_t z = y;
   int acc = 0;
   if (reject_row) {
-    const int32_t xd = rq.tokens[local];
+    const int32_t xd = rs.draft;
     const int qm = rs.qm;
+    // residual (p - q)+ over the kept entries; p(x) from the matching entry
     float px = 0.0f;
-    for (int jj = lane; jj < m; jj += 32) {
-      const float pj = __fdiv_rn(rs.e[jj], S);
-      float qj = 0.0f;
-      for (int s2 = 0; s2 < qm; ++s2)
-        if (rs.qid[s2] == rs.ids[jj]) qj = __fadd_rn(qj, rs.qp[s2]);
-      const float d = __fsub_rn(pj, qj);
-      rs.r[jj] = d > 0.0f ? d : 0.0f;
-      if (rs.ids[jj] == xd) px = pj;
+    for (int jj = lane; jj < kPool; jj += 32) {
+      float rj = 0.0f;
+      if (jj < m) {
+        const float pj = __fdiv_rn(rs.e[jj], S);
+        float qj = 0.0f;
+        for (int s2 = 0; s2 < qm; ++s2)
+          if (rs.qid[s2] == rs.ids[jj]) qj = __fadd_rn(qj, rs.qp[s2]);
+        const float d = __fsub_rn(pj, qj);
+        rj = d > 0.0f ? d : 0.0f;
+        if (rs.ids[jj] == xd) px = pj;
+      }
+      rs.r[jj] = rj;
     }
     // pool ids are distinct: at most one lane holds p(x)
     for (int o = 16; o >= 1; o >>= 1) {
@@ -345,19 +478,15 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
       float qx = 0.0f;
       for (int s2 = 0; s2 < qm; ++s2)
         if (rs.qid[s2] == xd) qx = __fadd_rn(qx, rs.qp[s2]);
-      const float u1 = uniform01(rq.seed, rq.position, urow, kPurposeAccept);
-      rs.acc = (qx > 0.0f) ? (__fmul_rn(u1, qx) < px) : (px > 0.0f);
-      float a = 0.0f;
-      for (int jj = 0; jj < m; ++jj) {
-        a = __fadd_rn(a, rs.r[jj]);
-        rs.pr[jj] = a;
-      }
+      rs.acc = (qx > 0.0f) ? (__fmul_rn(rs.u1, qx) < px) : (px > 0.0f);
+      running_sums(rs.r, rs.pr, m);
     }
     __syncwarp();
     acc = rs.acc;
-    const float sr = m ? rs.pr[m - 1] : 0.0f;
+    const float sr = rs.pr[m - 1];
     if (sr > 0.0f) {
-      int jz = first_above(rs.pr, m, __fmul_rn(u2, sr));
+      const float tz = __fmul_rn(u2, sr);
+      int jz = warp_first(m, [&](int i) { return rs.pr[i] > tz; });
       if (jz < 0) jz = last_positive(rs.r, m);
       z = rs.ids[jz];
     }
@@ -451,7 +580,7 @@ __device__ void accept_request(const ReqDev& rq, int vocab, const int4* dec, int
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// shared tail of the sampling kernels
 
 struct SampleArgs {
   const float* logits;     // [rows][vocab] (penalised where penalties apply)
@@ -466,56 +595,29 @@ struct SampleArgs {
   int decide;              // 0: pools only
 };
 
-__global__ void __launch_bounds__(THREADS)
-    sample_kernel(SampleArgs a, ReqTable tab) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  StageShared& st = *reinterpret_cast<StageShared*>(dyn_smem);
-  __shared__ RowShared rs;
-  __shared__ AcceptShared as;
-  __shared__ int last;
-  pdl_trigger();
-  pdl_wait();
-  const int seg = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
-  const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
-
-  // 1. the segment's top 64, stored in pool order
-  {
-    SelectShared& sh = st.sel;
-    const long long s0 = static_cast<long long>(seg) * a.seg_len;
-    const long long s1 = std::min<long long>(s0 + a.seg_len, a.vocab);
-    uint64_t carry = 0ull;
-    for (long long b = s0; b < s1; b += SUB) {
-      uint64_t x[ITEMS];
-#pragma unroll
-      for (int i = 0; i < SUB / THREADS; ++i) {
-        const long long e = b + i * THREADS + tid;
-        x[i] = (e < s1) ? composite_at(rp, e) : 0ull;
-      }
-      x[ITEMS - 1] = carry;
-      block_top64(x, sh);
-      carry = (tid < sh.count) ? sh.out[tid] : 0ull;
-      __syncthreads();
+// sh.out[0..count) -> sh.sorted in pool order (zero-padded)
+__device__ __forceinline__ void sort_out_into_sorted(SelectShared& sh) {
+  const int tid = threadIdx.x;
+  if (tid < kPool) {
+    uint64_t v = 0ull;
+    int rank = tid;
+    if (tid < sh.count) {
+      v = sh.out[tid];
+      rank = 0;
+      for (int j = 0; j < sh.count; ++j) rank += (sh.out[j] > v);
     }
-    if (tid < kPool) {
-      int rank = tid;
-      if (carry != 0ull) {
-        rank = 0;
-        for (int j = 0; j < sh.count; ++j) rank += (sh.out[j] > carry);
-      }
-      a.cand[(static_cast<size_t>(row) * a.nseg + seg) * kPool + rank] = carry;
-    }
+    sh.sorted[rank] = v;
   }
+  __syncthreads();
+}
 
-  // 2. the last segment of the row to finish builds the pool and decides
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&a.row_ticket[row], 1u) == static_cast<uint32_t>(a.nseg - 1);
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (tid == 0) a.row_ticket[row] = 0u;
-  const uint64_t* pool =
-      merge_lists(a.cand + static_cast<size_t>(row) * a.nseg * kPool, a.nseg, st.mrg);
+// The row's pool (64 composites in pool order, zero-padded) -> pool ids and
+// values, then the row's decisions, then (last row of its request) the
+// acceptance walk.
+__device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, const uint64_t* pool,
+                           RowShared& rs, AcceptShared& as, int& last) {
+  const int tid = threadIdx.x;
+  const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const int n = a.vocab < kPool ? a.vocab : kPool;
   if (tid < kPool) {
     int32_t id = -1;
@@ -535,7 +637,7 @@ __global__ void __launch_bounds__(THREADS)
   const ReqDev& rq = request(tab, b);
   decide_row(rq, row, n, rs, a.dec);
 
-  // 3. the last row of the request to finish walks the request
+  // the last row of the request to finish walks the request
   __threadfence();
   __syncthreads();
   if (tid == 0)
@@ -547,11 +649,153 @@ __global__ void __launch_bounds__(THREADS)
   accept_request(rq, a.vocab, a.dec, a.status, as);
 }
 
+// ---------------------------------------------------------------------------
+// the kernel
+
+
+__global__ void __launch_bounds__(THREADS)
+    sample_kernel(SampleArgs a, ReqTable tab) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  StageShared& st = *reinterpret_cast<StageShared*>(dyn_smem);
+  __shared__ RowShared rs;
+  __shared__ AcceptShared as;
+  __shared__ int last;
+  pdl_trigger();
+  pdl_wait();
+  const int seg = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
+  const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
+
+  // 1. the segment's top 64, stored in pool order
+  {
+    SelectShared& sh = st.sel;
+    const long long s0 = static_cast<long long>(seg) * a.seg_len;
+    const long long s1 = std::min<long long>(s0 + a.seg_len, a.vocab);
+    uint64_t carry = 0ull;            // thread t < 64: entry t of the running list
+    for (long long b = s0; b < s1; b += SUB) {
+      uint64_t x[ITEMS];
+#pragma unroll
+      for (int i = 0; i < SUB / THREADS; ++i) {
+        const long long e = b + i * THREADS + tid;
+        x[i] = (e < s1) ? composite_at(rp, e) : 0ull;
+      }
+      x[ITEMS - 1] = carry;
+      if (!block_top64_filtered(x, sh)) {
+        block_top64(x, sh);
+        sort_out_into_sorted(sh);
+      }
+      carry = (tid < kPool) ? sh.sorted[tid] : 0ull;
+      __syncthreads();
+    }
+    if (tid < kPool) a.cand[(static_cast<size_t>(row) * a.nseg + seg) * kPool + tid] = carry;
+  }
+
+  // 2. the last segment of the row to finish builds the pool and decides
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(&a.row_ticket[row], 1u) == static_cast<uint32_t>(a.nseg - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) a.row_ticket[row] = 0u;
+  const uint64_t* pool =
+      merge_lists(a.cand + static_cast<size_t>(row) * a.nseg * kPool, a.nseg, st.mrg);
+  finish_row(a, tab, row, pool, rs, as, last);
+}
+
+// Sampling stage for rows whose group maxima (largest order key per 32
+// vocabulary rows) were recorded by the projection: one CTA per row.
+//  (a) the row's 64 groups with the largest maxima (ties: lower group index),
+//      tau = the maximum of the 64th: at least 64 entries reach tau, and every
+//      entry of the row's top 64 lies in those groups at or above tau;
+//  (b) the chosen groups' entries at or above tau (at most 64 x 32) are
+//      gathered and their top 64 taken;
+//  (c) pool, policy, decisions and acceptance as in sample_kernel.
+__global__ void __launch_bounds__(THREADS, 1)
+    sample_rows_kernel(SampleArgs a, ReqTable tab, const uint32_t* __restrict__ gmax,
+                       int ngroups) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  RowsShared& sr = *reinterpret_cast<RowsShared*>(dyn_smem);
+  SelectShared& sh = sr.sel;
+  __shared__ RowShared rs;
+  __shared__ AcceptShared as;
+  __shared__ int last;
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
+  const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
+
+  // (a) top 64 groups, as composites (max key << 32) | ~group
+  {
+    uint64_t x[GI_MAX];
+#pragma unroll
+    for (int i = 0; i < GI_MAX; ++i) {
+      const int g = i * THREADS + tid;
+      x[i] = g < ngroups ? pack_key_id(gm[g], static_cast<uint32_t>(g)) : 0ull;
+    }
+    if (!block_top64_filtered(x, sh)) {
+      block_top64(x, sh);
+      sort_out_into_sorted(sh);
+    }
+  }
+  const int nchosen = ngroups < kPool ? ngroups : kPool;
+  const uint32_t tau = static_cast<uint32_t>(sh.sorted[nchosen - 1] >> 32);
+  if (tid == 0) sr.ccount = 0;
+  __syncthreads();
+
+  // (b) the chosen groups' entries at or above tau; a warp per group
+  for (int j = warp; j < nchosen; j += THREADS / 32) {
+    const uint32_t g = packed_id(sh.sorted[j]);
+    const long long v = static_cast<long long>(g) * 32 + lane;
+    uint64_t c = 0ull;
+    if (v < a.vocab) {
+      const uint32_t k = float_key(rp[v]);
+      if (k >= tau) c = pack_key_id(k, static_cast<uint32_t>(v));
+    }
+    const uint32_t ball = __ballot_sync(0xffffffffu, c != 0ull);
+    if (ball) {
+      int at = 0;
+      if (lane == 0) at = atomicAdd(&sr.ccount, __popc(ball));
+      at = __shfl_sync(0xffffffffu, at, 0);
+      if (c != 0ull) sr.cands[at + __popc(ball & ((1u << lane) - 1u))] = c;
+    }
+  }
+  __syncthreads();
+
+  // (c) their top 64, in pool order
+  const int n = sr.ccount;
+  uint64_t* pool = sr.pool;
+  if (n <= GATHER_MAX) {
+    if (tid < kPool) pool[tid] = 0ull;
+    __syncthreads();
+    if (tid < n) {
+      const uint64_t me = sr.cands[tid];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += (sr.cands[j] > me);
+      if (rank < kPool) pool[rank] = me;
+    }
+    __syncthreads();
+  } else {
+    uint64_t x[C_MAX / THREADS];
+#pragma unroll
+    for (int i = 0; i < C_MAX / THREADS; ++i) {
+      const int k = i * THREADS + tid;
+      x[i] = k < n ? sr.cands[k] : 0ull;
+    }
+    block_top64(x, sh);
+    sort_out_into_sorted(sh);
+    if (tid < kPool) pool[tid] = sh.sorted[tid];
+    __syncthreads();
+  }
+  finish_row(a, tab, row, pool, rs, as, last);
+}
+
 __global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len, vr_policy pol,
                               int32_t* __restrict__ out_m, float* __restrict__ out_e,
                               float* __restrict__ out_S) {
   __shared__ float vals[kPool];
-  __shared__ float e[kPool];
+  __shared__ __align__(16) float e[kPool];
+  __shared__ __align__(16) float pc[kPool];
   __shared__ int m;
   __shared__ float S;
   pdl_trigger();
@@ -559,7 +803,7 @@ __global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len,
   const int row = blockIdx.x;
   for (int j = threadIdx.x; j < kPool; j += 32) vals[j] = pool_vals[static_cast<size_t>(row) * kPool + j];
   __syncwarp();
-  policy_warp(vals, pool_len, pol, e, &m, &S);
+  policy_warp(vals, pool_len, pol, e, pc, &m, &S);
   for (int j = threadIdx.x; j < kPool; j += 32) out_e[static_cast<size_t>(row) * kPool + j] = e[j];
   if (threadIdx.x == 0) {
     out_m[row] = m;
@@ -609,6 +853,36 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   ReqTable none{};
   return launch_pdl(smp::sample_kernel, dim3(nseg, rows), dim3(smp::THREADS), smem, stream, a,
                     tab ? *tab : none) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
+bool sample_rows_supported(int vocab) {
+  return (vocab + 31) / 32 <= smp::GI_MAX * smp::THREADS;
+}
+
+int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t* gmax,
+                       uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
+                       const ReqTable& tab, int4* dec, int32_t* status, cudaStream_t stream) {
+  smp::SampleArgs a{};
+  a.logits = logits;
+  a.vocab = vocab;
+  a.req_ticket = req_ticket;
+  a.pool_ids = pool_ids;
+  a.pool_vals = pool_vals;
+  a.dec = dec;
+  a.status = status;
+  a.decide = 1;
+  const size_t smem = sizeof(smp::RowsShared);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(smp::sample_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return VR_ERR_CUDA;
+    attr_set = true;
+  }
+  return launch_pdl(smp::sample_rows_kernel, dim3(rows), dim3(smp::THREADS), smem, stream, a, tab,
+                    gmax, (vocab + 31) / 32) == cudaSuccess
              ? VR_OK
              : VR_ERR_CUDA;
 }

@@ -162,10 +162,14 @@ __device__ __forceinline__ float penalize_value(float x, int count, const vr_pol
 }
 
 // ---------------------------------------------------------------------------
-// sampler policy on one pool (values in pool order).  The e_j are computed
-// by the calling warp's lanes; lane 0 then runs the sequential min-p, top-p
-// and sum, in pool order.  e has room for kPool entries; entries past the
-// kept count are set to 0.
+// sampler policy on one pool (values in pool order), run by one warp.
+// The e_j are computed by the lanes; one lane then forms the running sums
+// pc[j] = e_0 + ... + e_j in pool order, one rounding per addition (the
+// sequential sums the policy is defined with).  Every later step reads them:
+// top-p's total over the min-p survivors is pc[m-1], its cut is the first j
+// with pc[j] >= top_p * pc[m-1], the final S is pc[m-1] of the kept prefix,
+// and a draw takes the first j with pc[j] > u * S.  e and pc have room for
+// kPool entries; e past the kept count is set to 0.
 
 __device__ __forceinline__ int topk_limit(int32_t top_k) {
   if (top_k < 0) return kTopKAbsent;
@@ -173,13 +177,49 @@ __device__ __forceinline__ int topk_limit(int32_t top_k) {
   return top_k < kPool ? top_k : kPool;
 }
 
+// smallest j < m with pred(j) over j = lane, lane + 32; -1 if none
+template <typename Pred>
+__device__ __forceinline__ int warp_first(int m, Pred pred) {
+  const int lane = threadIdx.x & 31;
+  uint32_t b = __ballot_sync(0xffffffffu, lane < m && pred(lane));
+  if (b) return __ffs(b) - 1;
+  b = __ballot_sync(0xffffffffu, lane + 32 < m && pred(lane + 32));
+  return b ? 32 + __ffs(b) - 1 : -1;
+}
+
+// running sums c[j] = w_0 + ... + w_j for j < n, sequential, by one lane;
+// w and c 16-byte aligned
+__device__ __forceinline__ void running_sums(const float* w, float* c, int n) {
+  float acc = 0.0f;
+  int j = 0;
+  for (; j + 4 <= n; j += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(w + j);
+    acc = __fadd_rn(acc, v.x);
+    c[j] = acc;
+    acc = __fadd_rn(acc, v.y);
+    c[j + 1] = acc;
+    acc = __fadd_rn(acc, v.z);
+    c[j + 2] = acc;
+    acc = __fadd_rn(acc, v.w);
+    c[j + 3] = acc;
+  }
+  for (; j < n; ++j) {
+    acc = __fadd_rn(acc, w[j]);
+    c[j] = acc;
+  }
+}
+
+// e and pc must be 16-byte aligned shared arrays of kPool floats
 __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_policy& pol,
-                                            float* e, int* m_out, float* S_out) {
+                                            float* e, float* pc, int* m_out, float* S_out) {
   const int lane = threadIdx.x & 31;
   int K = topk_limit(pol.top_k);
   if (K > n) K = n;
   if (pol.temperature == 0.f) {
-    for (int j = lane; j < kPool; j += 32) e[j] = (j == 0) ? 1.0f : 0.0f;
+    for (int j = lane; j < kPool; j += 32) {
+      e[j] = (j == 0) ? 1.0f : 0.0f;
+      pc[j] = 1.0f;
+    }
     __syncwarp();
     if (lane == 0) {
       *m_out = 1;
@@ -204,31 +244,25 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
     e[j] = ej;
   }
   __syncwarp();
+  if (lane == 0) running_sums(e, pc, K);
+  __syncwarp();
+  int m = K;
+  if (pol.min_p > 0.f) {
+    const float mp = pol.min_p;
+    const int j = warp_first(K, [&](int i) { return i >= 1 && e[i] < mp; });
+    if (j >= 1) m = j;
+  }
+  if (pol.top_p < 1.f) {
+    const float thr = __fmul_rn(pol.top_p, pc[m - 1]);
+    const int j = warp_first(m, [&](int i) { return pc[i] >= thr; });
+    if (j >= 0) m = j + 1;
+  }
+  __syncwarp();
+  for (int j = lane; j < kPool; j += 32)
+    if (j >= m) e[j] = 0.0f;
   if (lane == 0) {
-    int m = K;
-    if (pol.min_p > 0.f) {
-      int j = 1;
-      while (j < m && e[j] >= pol.min_p) ++j;
-      m = j;
-    }
-    if (pol.top_p < 1.f) {
-      float s = 0.0f;
-      for (int j = 0; j < m; ++j) s = __fadd_rn(s, e[j]);
-      const float thr = __fmul_rn(pol.top_p, s);
-      float c = 0.0f;
-      for (int j = 0; j < m; ++j) {
-        c = __fadd_rn(c, e[j]);
-        if (c >= thr) {
-          m = j + 1;
-          break;
-        }
-      }
-    }
-    float S = 0.0f;
-    for (int j = 0; j < m; ++j) S = __fadd_rn(S, e[j]);
-    for (int j = m; j < kPool; ++j) e[j] = 0.0f;
     *m_out = m;
-    *S_out = S;
+    *S_out = pc[m - 1];
   }
   __syncwarp();
 }

@@ -15,17 +15,21 @@ bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64
                       uint32_t box_inner, uint32_t box_outer);
 size_t tc_plane_bytes(int rows, int hidden);
 size_t tcb_plane_bytes(int rows, int hidden);
+// gmax (nullable): [rows][ceil(vocab/32)] largest order key per 32 vocab rows
 int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                       float* logits, void* planes, int32_t* status, cudaStream_t stream);
+                       float* logits, void* planes, uint32_t* gmax, int32_t* status,
+                       cudaStream_t stream);
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                      float* logits, void* planes, int32_t* status, cudaStream_t stream);
+                      float* logits, void* planes, uint32_t* gmax, int32_t* status,
+                      cudaStream_t stream);
 int ffma_rows_per_pass(int hidden);
 int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                         float* logits, cudaStream_t stream);
 
 // penalties: rows_total rows of `logits` (stride vocab), requests in `tab`
+// gmax (nullable): group maxima of `logits`, refreshed for the touched groups
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab,
-                    bool with_q, int32_t* status, cudaStream_t stream);
+                    bool with_q, uint32_t* gmax, int32_t* status, cudaStream_t stream);
 
 // sampling stage, one kernel: logits [rows][vocab] -> pool ids/vals
 // [rows][64]; with a request table also the policy, the per-row decisions
@@ -37,6 +41,13 @@ size_t select_cand_bytes(int rows, int vocab);
 int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
                   uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
                   int4* dec, int32_t* status, cudaStream_t stream);
+
+// the same stage for rows whose group maxima gmax [rows][ceil(vocab/32)]
+// (largest order key per 32 vocabulary rows) are known: one CTA per row
+bool sample_rows_supported(int vocab);
+int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t* gmax,
+                       uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
+                       const ReqTable& tab, int4* dec, int32_t* status, cudaStream_t stream);
 
 int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
                   int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream);
