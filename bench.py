@@ -48,9 +48,11 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the penalised-chain, tree and batched workloads")
-    p.add_argument("--mode", choices=["full", "window", "project"], default="full",
+    p.add_argument("--mode", choices=["full", "window", "project", "project_batched"],
+                   default="full",
                    help="window: only the timed windows (for a profiler's launch list); "
-                        "project: only the projection of one window (for a kernel capture)")
+                        "project: only the projection of one window (for a kernel capture); "
+                        "project_batched: only the 256-row batched projection at hidden 5120")
     return p.parse_args()
 
 
@@ -360,6 +362,25 @@ def run_projection_only(torch, vb, synth, wd, dev, args):
                       "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
 
 
+def run_batched_projection_only(torch, vb, synth, dev, args):
+    """The batched-serving projection (256 rows, hidden 5120, tensor-core batch
+    path), warm-up + steps times."""
+    H5, R = 5120, 256
+    wd5 = torch.from_numpy(synth.weights(V, H5).view(np.int16)).to(dev)
+    a = torch.from_numpy(synth.activations(R, H5, 500)).to(dev)
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    ws = vb.workspace(R, H5, V, device=dev)
+    for _ in range(args.warmup):
+        vb.verify_project(wd5, a, lg, ws, path=vb.VR_PATH_TC_BATCH)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vb.verify_project(wd5, a, lg, ws, path=vb.VR_PATH_TC_BATCH)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"mode": "project_batched", "steps": args.steps,
+                      "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -375,6 +396,9 @@ def main():
     vbuild.build()
     vb.lib()
 
+    if args.mode == "project_batched":
+        run_batched_projection_only(torch, vb, synth, dev, args)
+        return
     W = synth.weights(V, H)
     wd = torch.from_numpy(W.view(np.int16)).to(dev)
     if args.mode == "project":
