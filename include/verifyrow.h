@@ -230,15 +230,18 @@ VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, cons
  *     then the argmax at the first mismatch or the bonus after the last row
  *     (§02); tree -> the deepest node whose whole path agrees with the
  *     argmax of each parent row (equal depths: the lower node index).
- *   sampled chain with q_ids/q_logits (penalised by the caller):
- *     rejection sampling (§03): accept d_i iff u1 * q_i(d_i) < p_i(d_i)
- *     (q_i(d_i) = 0: iff p_i(d_i) > 0); on rejection emit a draw from
- *     (p_i - q_i)+ renormalised (from p_i if that is all zero) and stop; after
- *     k acceptances draw the bonus from p_k.  q_i is the same policy on the
- *     8 candidates of node i ordered like the pool.
- *   sampled tree, or sampled chain without q: naive sampling descent: from
- *     the root draw y ~ p(row); move to the lowest-index child carrying y,
- *     else emit y and stop.
+ *   sampled chain: rejection sampling (§03): accept d_i iff
+ *     u1 * q_i(d_i) < p_i(d_i) (q_i(d_i) = 0: iff p_i(d_i) > 0); on rejection
+ *     emit a draw from (p_i - q_i)+ renormalised (from p_i if that is all
+ *     zero) and stop; after k acceptances draw the bonus from p_k.
+ *     With q_ids/q_logits (penalised by the caller), q_i is the same policy
+ *     on the 8 candidates of node i ordered like the pool.  Without them
+ *     (q_ids == NULL: drafts proposed without probabilities, such as n-gram
+ *     matches), q_i = delta(d_i) (§06 "N-gram takeovers"): d_i is accepted
+ *     iff u1 < p_i(d_i), and the replacement is drawn from p_i with d_i
+ *     removed.
+ *   sampled tree: naive sampling descent: from the root draw y ~ p(row);
+ *     move to the lowest-index child carrying y, else emit y and stop.
  * Draws: u = Philox4x64-10(counter = (position, row, purpose, 0),
  * key = (seed, 0)) word 0 >> 40, times 2^-24 (a float32); purpose 1 = accept
  * uniform, 2 = emitted draw; t = u * S picks the first j whose running sum

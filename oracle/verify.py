@@ -417,13 +417,23 @@ def accept_rejection_chain(pdists, qdists, drafts, uniforms, replacement="residu
     return emitted, k
 
 
+def point_mass(token):
+    """q = delta(token): the draft distribution of a candidate proposed
+    without probabilities (an n-gram match).  Fed to the chain rejection test
+    it accepts the token with probability p(token) and, on rejection, draws
+    from p with the token removed ("Speculative decoding on RDNA" §06, N-gram
+    takeovers: sampled candidates take the same rejection test with a
+    point-mass draft)."""
+    return RowDist([int(token)], [F32(1.0)], F32(1.0))
+
+
 def accept_naive_descent(pdists, tokens, parent, uniforms):
     """Naive sampling verify, exact for any deterministic draft ("feat(dflash)
     ...", notes under the spec-step listing): from the root, draw y from the
     current row's p; if a child of the current node carries y (reading: the
     lowest-index such child), move there and repeat; otherwise emit y and
     stop.  At a leaf the draw is the bonus token.  Used for sampled token
-    trees and for sampled chains given without draft candidates."""
+    trees."""
     children = {}
     for j, p in enumerate(parent):
         children.setdefault(int(p), []).append(j)
@@ -453,7 +463,8 @@ class WindowResult:
     pool_ids: list                  # per row, int64 [min(64, V)]
     pool_vals: list                 # per row, float32
     pdists: list                    # per row RowDist
-    qdists: list                    # per node RowDist (chain rejection only)
+    qdists: list                    # per node RowDist (chain rejection only;
+                                    # point masses when no candidates were given)
     q_pen: np.ndarray = None        # [n, C] penalised draft logits
     emitted: list = field(default_factory=list)
     accept: int = 0
@@ -498,10 +509,11 @@ def verify_window(logits, tokens, parent=None, q_ids=None, q_logits=None, hist=(
     """One speculative window on given target logits [R, V] (float32).
 
     tokens: draft tokens (chain) or node tokens (tree); parent None = chain.
-    Greedy requests: accept_greedy.  Sampled chains with draft candidates:
-    rejection sampling.  Sampled trees, and sampled chains without draft
-    candidates: naive sampling descent.  Every window emits at least one
-    token ("Speculative decoding on RDNA" §01)."""
+    Greedy requests: accept_greedy.  Sampled chains: rejection sampling,
+    against the draft candidates' q when given, else against the point mass
+    on each draft (n-gram takeover).  Sampled trees: naive sampling descent.
+    Every window emits at least one token ("Speculative decoding on RDNA"
+    §01)."""
     pol = pol or Policy()
     tokens = [int(t) for t in tokens]
     parent = chain_parents(len(tokens)) if parent is None else [int(p) for p in parent]
@@ -512,7 +524,9 @@ def verify_window(logits, tokens, parent=None, q_ids=None, q_logits=None, hist=(
     if pol.greedy:
         argmax = [int(ids[0]) for ids in res.pool_ids]
         res.emitted, res.accept = accept_greedy(argmax, tokens, parent)
-    elif q_ids is not None and is_chain(parent):
+    elif is_chain(parent):
+        if q_ids is None:
+            res.qdists = [point_mass(t) for t in tokens]
         res.emitted, res.accept = accept_rejection_chain(res.pdists, res.qdists, tokens,
                                                          uniforms, replacement)
     else:

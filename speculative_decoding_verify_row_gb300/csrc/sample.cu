@@ -21,8 +21,9 @@
 //  3. that CTA then takes a ticket on the request's counter; the last row of
 //     the request to finish walks the request's rows and writes the emitted
 //     ids (greedy prefix or longest tree branch, §02; rejection sampling,
-//     §03 steps 1-4; naive descent for deterministic tree drafts, "feat(dflash)
-//     ...").
+//     §03 steps 1-4, against the draft candidates' q or, for drafts proposed
+//     without probabilities, q = delta(draft), §06; naive descent for
+//     deterministic tree drafts, "feat(dflash) ...").
 // Tickets follow a __threadfence() after the CTA's writes, so the last CTA
 // sees all of them (the usual threadfence-reduction pattern).
 #include <algorithm>
@@ -408,11 +409,20 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
     for (int j = tid; j < rq.n_nodes; j += THREADS)
       if (rq.parent[j] != j - 1) rs.chain = 0;
   __syncthreads();
-  const bool reject_row = rq.q_ids != nullptr && rs.chain && local < rq.n_nodes;
+  // sampled chains take the rejection test: against the draft candidates' q
+  // when given, else against q = delta(draft) (a candidate proposed without
+  // probabilities, e.g. by an n-gram match)
+  const bool reject_row = rs.chain && local < rq.n_nodes;
   const uint64_t urow = static_cast<uint64_t>(local);
 
   if (warp == 0) {
     policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
+  } else if (warp == 1 && reject_row && !rq.q_ids) {
+    if (lane == 0) {
+      rs.qid[0] = rq.tokens[local];
+      rs.qp[0] = 1.0f;
+      rs.qm = 1;
+    }
   } else if (warp == 1 && reject_row) {
     // q: the node's candidates in pool order, then the same policy
     const float* qv = rq.q_pen + static_cast<size_t>(local) * kQCand;
@@ -519,8 +529,8 @@ __device__ void accept_request(const ReqDev& rq, int vocab, const int4* dec, int
     if (b) atomicOr(&as.bad, b);
   }
   __syncthreads();
-  const bool rejection = !greedy && rq.q_ids != nullptr && !as.not_chain;
-  if (rejection)
+  const bool rejection = !greedy && !as.not_chain;
+  if (rejection && rq.q_ids)
     for (int i = tid; i < n * kQCand; i += THREADS) {
       const int id = rq.q_ids[i];
       if (id < 0 || id >= vocab) atomicOr(&as.bad, VR_DEV_BAD_QID);

@@ -1,6 +1,6 @@
 """GPU penalty prepass and acceptance, bit for bit against the oracle given
-the same logits ("Speculative decoding on RDNA" §02-§04; token trees and
-naive sampling verify from the other two pages)."""
+the same logits ("Speculative decoding on RDNA" §02-§04, point-mass drafts
+§06; token trees and naive sampling verify from the other two pages)."""
 import numpy as np
 import pytest
 import torch
@@ -133,3 +133,32 @@ def test_invalid_device_data_sets_the_status_word():
     # a good window afterwards is unaffected
     _, acc, ne, st = gpu_accept(pen, np.int32([0, 0]), None, None, None, ov.Policy(), 0, 0)
     assert ne == 3 and st == 0
+
+
+def test_point_mass_drafts_match_one_finite_candidate():
+    """Sampled chains without candidates take q = delta(draft); the same
+    window given 8 candidates of which only the draft is finite must emit the
+    same tokens, and both must match the oracle."""
+    rng = np.random.default_rng(77)
+    V = 2000
+    pol = ov.Policy(temperature=0.8, top_k=0, min_p=0.02, top_p=0.95)
+    accepted = rejected = 0
+    for trial in range(60):
+        n = int(rng.integers(1, 9))
+        pen = (rng.standard_normal((n + 1, V)) * 2).astype(np.float32)
+        top = np.argsort(-pen, axis=1)[:, :4]
+        tokens = np.array([top[j, int(rng.integers(0, 4))] for j in range(n)], np.int32)
+        q_ids = rng.integers(0, V, (n, 8)).astype(np.int32)
+        q_ids[:, 0] = tokens
+        q_log = np.full((n, 8), -np.inf, np.float32)
+        q_log[:, 0] = rng.standard_normal(n).astype(np.float32)
+        seed, position = int(rng.integers(0, 2**63)), int(rng.integers(0, 10**6))
+        a = gpu_accept(pen, tokens, None, None, None, pol, seed, position)
+        b = gpu_accept(pen, tokens, None, q_ids, q_log, pol, seed, position)
+        ref = ov.verify_window(pen, tokens, None, None, None, (), pol, seed, position)
+        assert a[3] == 0 and b[3] == 0
+        assert (a[1], a[2]) == (ref.accept, ref.n_emitted) == (b[1], b[2])
+        assert list(a[0][:a[2]]) == ref.emitted == list(b[0][:b[2]])
+        accepted += ref.accept
+        rejected += ref.accept < n
+    assert accepted > 20 and rejected > 20

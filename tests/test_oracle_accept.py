@@ -255,3 +255,122 @@ def test_invalid_trees_are_rejected():
         ov.verify_window(logits, [1, 2], [-1, 1])       # parent is not an earlier node
     with pytest.raises(ValueError):
         ov.verify_window(logits, [1, 9], [-1, 0])       # token outside the vocabulary
+
+
+def _point_mass_breakpoints(prep, p_ref, drafts, k):
+    """Jumps of the point-mass chain rule: u1 at p(x); u2 at the running sums
+    of p and of p with the draft removed, both in pool order."""
+    def bp(key):
+        row, purpose = key
+        pd = prep.pdists[row]
+        order = [pd.ids[j] for j in range(pd.m)]
+        if purpose == PURPOSE_ACCEPT:
+            return [p_ref[row][drafts[row]]]
+        pts = list(np.cumsum(p_ref[row][order]))
+        if row < k:
+            r = np.where(np.array(order) == drafts[row], 0.0, p_ref[row][order])
+            if r.sum() > 0:
+                pts += list(np.cumsum(r) / r.sum())
+        return pts
+    return bp
+
+
+@pytest.mark.parametrize("V,k,T,seed", [(6, 2, 1.0, 40), (5, 3, 0.6, 41), (7, 2, 1.4, 42)])
+def test_point_mass_drafts_are_exact_by_enumeration(V, k, T, seed):
+    """Drafts proposed without probabilities ("Speculative decoding on RDNA"
+    §06, n-gram takeovers): accept d_i with probability p_i(d_i), else draw
+    from p_i without d_i.  Exact law over every uniform: the first token
+    follows p_0 and, given the window reached depth j, the token there
+    follows p_j."""
+    rng = np.random.default_rng(seed)
+    logits = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    drafts = [int(np.argmax(logits[i])) if i % 2 == 0 else int(rng.integers(0, V)) for i in range(k)]
+    pol = ov.Policy(temperature=T, top_k=0)
+    prep = ov.prepare_rows(logits, drafts, ov.chain_parents(k), None, None, [], pol)
+    p_ref = [softmax(logits[r].astype(np.float64) / np.float64(np.float32(T))) for r in range(k + 1)]
+    q = [ov.point_mass(d) for d in drafts]
+
+    def run(u):
+        return tuple(ov.accept_rejection_chain(prep.pdists, q, drafts, u)[0])
+    law = _explore(run, _point_mass_breakpoints(prep, p_ref, drafts, k))
+    first = np.zeros(V)
+    reach = np.zeros(k + 1)
+    at_depth = np.zeros((k + 1, V))
+    for em, w in law.items():
+        first[em[0]] += w
+        for d, t in enumerate(em):
+            reach[d] += w
+            at_depth[d, t] += w
+    assert abs(first.sum() - 1.0) < 1e-9
+    np.testing.assert_allclose(first, p_ref[0], atol=2e-6)
+    # depth d is reached exactly when d_0..d_{d-1} were all accepted
+    for d in range(1, k + 1):
+        np.testing.assert_allclose(reach[d], np.prod([p_ref[i][drafts[i]] for i in range(d)]),
+                                   atol=2e-6)
+        if reach[d] > 1e-3:
+            np.testing.assert_allclose(at_depth[d] / reach[d], p_ref[d], atol=2e-5)
+
+
+def test_point_mass_chain_has_the_law_of_naive_descent():
+    """For a fixed chain the point-mass rejection rule and naive sampling
+    descent (exact for any deterministic draft) emit every sequence with the
+    same probability, though from different uniforms."""
+    rng = np.random.default_rng(43)
+    V, k, T = 5, 3, 0.8
+    logits = (rng.standard_normal((k + 1, V)) * 1.2).astype(np.float32)
+    drafts = [int(np.argmax(logits[0])), int(np.argsort(logits[1])[-2]), int(np.argmax(logits[2]))]
+    pol = ov.Policy(temperature=T, top_k=0)
+    parent = ov.chain_parents(k)
+    prep = ov.prepare_rows(logits, drafts, parent, None, None, [], pol)
+    p_ref = [softmax(logits[r].astype(np.float64) / np.float64(np.float32(T))) for r in range(k + 1)]
+    q = [ov.point_mass(d) for d in drafts]
+    bp = _point_mass_breakpoints(prep, p_ref, drafts, k)
+    law_pm = _explore(lambda u: tuple(ov.accept_rejection_chain(prep.pdists, q, drafts, u)[0]), bp)
+    law_nd = _explore(lambda u: tuple(ov.accept_naive_descent(prep.pdists, drafts, parent, u)[0]), bp)
+    keys = set(law_pm) | set(law_nd)
+    assert len(keys) > 10
+    for s in keys:
+        assert abs(law_pm.get(s, 0.0) - law_nd.get(s, 0.0)) < 2e-6, s
+
+
+def test_point_mass_equals_candidates_with_one_finite_logit():
+    """q given as 8 candidates of which only the draft has a finite logit is
+    the point mass: same emitted tokens from the same uniforms, under
+    truncating policies and penalties."""
+    rng = np.random.default_rng(44)
+    for trial in range(400):
+        V = int(rng.integers(2, 60))
+        k = int(rng.integers(1, 7))
+        logits = (rng.standard_normal((k + 1, V)) * 2).astype(np.float32)
+        drafts = [int(np.argmax(logits[i])) if rng.random() < 0.5 else int(rng.integers(0, V))
+                  for i in range(k)]
+        pol = ov.Policy(temperature=float(rng.choice([0.3, 0.7, 1.0, 1.5])),
+                        top_k=int(rng.integers(-1, 70)), min_p=float(rng.choice([0.0, 0.05])),
+                        top_p=float(rng.choice([1.0, 0.9])), repeat=1.1, presence=1.5,
+                        frequency=0.2, window=int(rng.integers(0, 8)))
+        hist = list(rng.integers(0, V, 10))
+        qids = rng.integers(0, V, (k, 8))
+        qids[:, 0] = drafts
+        qlog = np.full((k, 8), -np.inf, np.float32)
+        qlog[:, 0] = rng.standard_normal(k).astype(np.float32)
+        a = ov.verify_window(logits, drafts, None, None, None, hist, pol, seed=trial, position=3)
+        b = ov.verify_window(logits, drafts, None, qids, qlog, hist, pol, seed=trial, position=3)
+        assert (a.emitted, a.accept) == (b.emitted, b.accept)
+
+
+def test_point_mass_accepts_with_probability_p_and_never_redraws_the_draft():
+    p = [_dist([0, 1, 2], [0.5, 0.3, 0.2]), _dist([0], [1.0])]
+    q = [ov.point_mass(1)]
+    S = float(p[0].total)
+    # accepted iff u1 < p(1) = 0.3
+    for u1, acc in ((0.2999, 1), (0.3001, 0)):
+        _, a = ov.accept_rejection_chain(p, q, [1], lambda r, k: u1 if k == PURPOSE_ACCEPT else 0.5)
+        assert a == acc
+    # on rejection the replacement is never the draft
+    for u2 in np.linspace(0.0, 0.999, 101):
+        em, a = ov.accept_rejection_chain(p, q, [1], lambda r, k: 0.9 if k == PURPOSE_ACCEPT else u2)
+        assert a == 0 and em[0] in (0, 2)
+    # a draft outside the kept set is rejected and p is drawn unchanged
+    em, a = ov.accept_rejection_chain(p, [ov.point_mass(7)], [7],
+                                      lambda r, k: 0.0 if k == PURPOSE_ACCEPT else 0.95)
+    assert a == 0 and em == [2] and S > 0

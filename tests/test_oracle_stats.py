@@ -95,3 +95,39 @@ def test_rejection_sampling_follows_p(name):
 def test_replacement_from_p_control_fails(name):
     prep, first, second = _simulate(name, "p")
     assert _chi2_p(first, prep.pdists[0]) < 1e-9
+
+
+def _simulate_point_mass(replacement):
+    """Fixed drafts proposed without probabilities (an n-gram takeover,
+    "Speculative decoding on RDNA" §06) through the rejection test with
+    q = delta(draft)."""
+    rng = np.random.default_rng(4)
+    V, k = 30, 2
+    logits = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    pol = ov.Policy(temperature=0.8, top_k=0, min_p=0.02, top_p=0.95)
+    drafts = [int(np.argmax(logits[0])), int(np.argsort(logits[1])[-2])]
+    prep = ov.prepare_rows(logits, drafts, ov.chain_parents(k), None, None, [], pol)
+    q = [ov.point_mass(d) for d in drafts]
+    seeds = np.arange(TRIALS, dtype=np.uint64)
+    u = {(r, pu): uniform_array(seeds, POSITION, r, pu)
+         for r in range(k + 1) for pu in (PURPOSE_ACCEPT, PURPOSE_EMIT)}
+    first, second = [], []
+    for t in range(TRIALS):
+        em, _ = ov.accept_rejection_chain(prep.pdists, q, drafts, lambda r, pu: u[(r, pu)][t],
+                                          replacement)
+        first.append(em[0])
+        if len(em) > 1:
+            second.append(em[1])
+    return prep, np.array(first), np.array(second)
+
+
+def test_point_mass_rejection_follows_p():
+    prep, first, second = _simulate_point_mass("residual")
+    assert _chi2_p(first, prep.pdists[0]) > 1e-4
+    assert len(second) > 1000
+    assert _chi2_p(second, prep.pdists[1]) > 1e-4
+
+
+def test_point_mass_replacement_from_p_control_fails():
+    prep, first, _ = _simulate_point_mass("p")
+    assert _chi2_p(first, prep.pdists[0]) < 1e-9
