@@ -216,13 +216,21 @@ def order_keys(vals):
     return keys
 
 
-def target_pool(row):
-    """Top-min(64, V) of a row: (ids int64, values float32) in pool order."""
+def top_k_entries(row, k):
+    """The first min(k, V) entries of a row in pool order: (ids int64,
+    values float32).  With k = 16 this is the batched top-K of "feat(dflash):
+    developer-only online draft tuning" (ties, NaN and -inf under one fixed
+    order)."""
     row = np.asarray(row, dtype=np.float32)
     keys = order_keys(row).astype(np.int64)
     ids = np.arange(row.shape[0], dtype=np.int64)
-    order = np.lexsort((ids, -keys))[:min(POOL, row.shape[0])]
+    order = np.lexsort((ids, -keys))[:min(k, row.shape[0])]
     return order, row[order]
+
+
+def target_pool(row):
+    """Top-min(64, V) of a row: (ids int64, values float32) in pool order."""
+    return top_k_entries(row, POOL)
 
 
 def candidate_pool(cand_ids, cand_vals):

@@ -278,6 +278,19 @@ int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids
                        nullptr, at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream));
 }
 
+int vr_topk(const float* x, int rows, int vocab, int k, int32_t* ids, float* vals, void* ws,
+            size_t ws_bytes, void* stream) {
+  int st = check_shape(rows, 8, vocab);
+  if (st != VR_OK) return st;
+  if (!x || !ids || !vals || k < 1 || k > VR_POOL) return VR_ERR_ARG;
+  if ((st = check_ws(ws, ws_bytes, rows, 8, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, 8, vocab);
+  return launch_sample(x, rows, vocab, at<uint64_t>(ws, L.cand),
+                       at<uint32_t>(ws, L.status + kRowTicketOff),
+                       at<uint32_t>(ws, L.status + kReqTicketOff), ids, vals, nullptr, nullptr,
+                       at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), k);
+}
+
 int vr_verify_policy(const float* pool_vals, int rows, int pool_len, const vr_policy* policy,
                      int32_t* out_m, float* out_e, float* out_S, void* stream) {
   int st = check_policy(policy);

@@ -598,8 +598,9 @@ struct SampleArgs {
   uint64_t* cand;          // [rows][nseg][64]
   uint32_t* row_ticket;    // [rows], zero between calls
   uint32_t* req_ticket;    // [requests], zero between calls
-  int32_t* pool_ids;       // [rows][64]
-  float* pool_vals;        // [rows][64]
+  int32_t* pool_ids;       // [rows][out_k]
+  float* pool_vals;        // [rows][out_k]
+  int out_k;               // leading pool entries written per row (<= 64)
   int4* dec;               // [rows]
   int32_t* status;
   int decide;              // 0: pools only
@@ -636,8 +637,10 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
       id = static_cast<int32_t>(packed_id(pool[tid]));
       v = rp[id];
     }
-    a.pool_ids[static_cast<size_t>(row) * kPool + tid] = id;
-    a.pool_vals[static_cast<size_t>(row) * kPool + tid] = v;
+    if (tid < a.out_k) {
+      a.pool_ids[static_cast<size_t>(row) * a.out_k + tid] = id;
+      a.pool_vals[static_cast<size_t>(row) * a.out_k + tid] = v;
+    }
     rs.ids[tid] = id;
     rs.vals[tid] = v;
   }
@@ -836,7 +839,8 @@ size_t select_cand_bytes(int rows, int vocab) {
 
 int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
                   uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
-                  int4* dec, int32_t* status, cudaStream_t stream) {
+                  int4* dec, int32_t* status, cudaStream_t stream, int out_k) {
+  if (out_k < 1 || out_k > kPool) return VR_ERR_ARG;
   const int nseg = select_segments(vocab);
   const long long per = (static_cast<long long>(vocab) + nseg - 1) / nseg;
   smp::SampleArgs a;
@@ -849,6 +853,7 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.req_ticket = req_ticket;
   a.pool_ids = pool_ids;
   a.pool_vals = pool_vals;
+  a.out_k = out_k;
   a.dec = dec;
   a.status = status;
   a.decide = tab ? 1 : 0;
@@ -880,6 +885,7 @@ int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t*
   a.req_ticket = req_ticket;
   a.pool_ids = pool_ids;
   a.pool_vals = pool_vals;
+  a.out_k = kPool;
   a.dec = dec;
   a.status = status;
   a.decide = 1;

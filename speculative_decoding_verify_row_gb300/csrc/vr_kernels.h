@@ -38,9 +38,11 @@ int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int voca
 // [requests] must be zero on entry and are zero again on exit.
 int select_segments(int vocab);
 size_t select_cand_bytes(int rows, int vocab);
+// out_k: entries written per row to pool_ids/pool_vals (row stride out_k);
+// the decisions always use the whole 64-wide pool.
 int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
                   uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
-                  int4* dec, int32_t* status, cudaStream_t stream);
+                  int4* dec, int32_t* status, cudaStream_t stream, int out_k = kPool);
 
 // the same stage for rows whose group maxima gmax [rows][ceil(vocab/32)]
 // (largest order key per 32 vocabulary rows) are known: one CTA per row

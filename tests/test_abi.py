@@ -75,3 +75,8 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert lib.vr_verify_window(p, p, 65, 4096, 100, 0, p, None, 64, None, None, None, 0,
                                 ctypes.byref(good), 0, 0, p, None, p, p, p, p, 1 << 30, None) == -1
     assert lib.vr_verify_policy(p, 4, 65, ctypes.byref(good), p, p, p, None) == -1
+    # top-K width in [1, 64]
+    for k in (0, 65, -3):
+        assert lib.vr_topk(p, 15, 248320, k, p, p, p, 1 << 30, None) == -1
+    assert lib.vr_topk(p, 15, 248320, 16, None, p, p, 1 << 30, None) == -1
+    assert lib.vr_topk(p, 15, 248320, 16, p, p, p, 64, None) == -5

@@ -108,3 +108,44 @@ def test_policy_bit_exact(pi, pool_len):
         assert np.array_equal(e[r, :rm].view(np.uint32), np.array(re, np.float32).view(np.uint32))
         assert np.all(e[r, rm:] == 0.0)
         assert np.float32(S[r]).view(np.uint32) == np.float32(rS).view(np.uint32)
+
+
+def gpu_topk(x, k):
+    R, V = x.shape
+    ids = torch.full((R, k), -7, dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    ws = vb.workspace(R, 8, V)
+    vb.topk(dev(x), k, ids, vals, ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), vals.cpu().numpy()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_byte_identity_15x248320(seed):
+    """The draft tuner's batched top-K ("feat(dflash) ...": 15 rows x 248320,
+    K = 16, ties, NaN and -inf): ids and value bytes identical to the
+    oracle."""
+    x = adversarial_rows(15, 248320, seed)
+    if seed % 4 == 0:                   # a tie block straddling the 16th place
+        x[:, 1000:1040] = x.max()
+    ids, vals = gpu_topk(x, 16)
+    for r in range(15):
+        ref_ids, ref_vals = ov.top_k_entries(x[r], 16)
+        assert np.array_equal(ids[r], ref_ids), r
+        assert np.array_equal(vals[r].view(np.uint32), ref_vals.view(np.uint32)), r
+
+
+@pytest.mark.parametrize("k", [1, 7, 16, 33, 64])
+@pytest.mark.parametrize("V", [5, 64, 4097, 248320])
+def test_topk_widths(k, V):
+    x = adversarial_rows(4, V, 7 * k + V)
+    ids, vals = gpu_topk(x, k)
+    n = min(k, V)
+    for r in range(4):
+        ref_ids, ref_vals = ov.top_k_entries(x[r], k)
+        assert np.array_equal(ids[r, :n], ref_ids)
+        assert np.array_equal(vals[r, :n].view(np.uint32), ref_vals.view(np.uint32))
+        assert np.all(ids[r, n:] == -1)
+    if k == 64:
+        pid, pval = gpu_pool(x)
+        assert np.array_equal(pid, ids) and np.array_equal(pval.view(np.uint32), vals.view(np.uint32))

@@ -130,3 +130,21 @@ def test_draw_matches_weights():
         counts[ov.draw_index(e, S, (i + 0.5) / N)] += 1
     np.testing.assert_allclose(counts / N, np.array(e, np.float64) / float(S), atol=2.0 / N)
     assert ov.draw_index(e, S, np.float32(1.0 - 2**-24)) == 4
+
+
+def test_top_k_entries_is_a_prefix_of_the_sorted_row():
+    """Top-K by brute force: Python's sort on (order key desc, id asc)."""
+    rng = np.random.default_rng(70)
+    for trial in range(200):
+        V = int(rng.integers(1, 40))
+        x = rng.choice(np.float32([np.nan, -np.inf, np.inf, 0.0, -0.0, 1.0, -2.5, 7.0]), V)
+        k = int(rng.integers(1, 70))
+        def key(i):
+            b = int(x[i:i + 1].view(np.uint32)[0])
+            if np.isnan(x[i]):
+                return (-1, -i)
+            return ((b ^ 0xFFFFFFFF) if b >> 31 else (b | 0x80000000), -i)
+        want = sorted(range(V), key=key, reverse=True)[:k]
+        ids, vals = ov.top_k_entries(x, k)
+        assert list(ids) == want
+        assert np.array_equal(vals.view(np.uint32), x[want].view(np.uint32))
