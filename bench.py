@@ -48,11 +48,12 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the penalised-chain, tree and batched workloads")
-    p.add_argument("--mode", choices=["full", "window", "project", "project_batched"],
+    p.add_argument("--mode", choices=["full", "window", "project", "project_batched", "topk"],
                    default="full",
                    help="window: only the timed windows (for a profiler's launch list); "
                         "project: only the projection of one window (for a kernel capture); "
-                        "project_batched: only the 256-row batched projection at hidden 5120")
+                        "project_batched: only the 256-row batched projection at hidden 5120; "
+                        "topk: only the batched top-K (15 x 248320, K 16)")
     return p.parse_args()
 
 
@@ -343,7 +344,117 @@ def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
                                  "executed_tflops": 2 * flops / tp / 1e12,
                                  "weight_gbs": V * H5 * 2 / tp / 1e9}
     del wd5
+    out["topk_15x248320_k16"] = topk_workload(torch, vb, dev, stream, n_steps)
     return out
+
+
+COST_ROWS = (1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 17, 21, 25)
+
+
+def window_cost_model(torch, vb, synth, wd, dev, stream):
+    """Window cost against rows, and what it implies for the draft depth
+    ("Speculative decoding on RDNA" §05).  Sampled chain windows with k
+    point-mass drafts (prompt-lookup style, no candidates) at 1..25 rows,
+    events on the stream, 64 windows per row count over 8 distinct inputs;
+    the library's cost fit ms = a + b (rows - 1) over those times; the
+    break-even tokens per window (cost / one-row cost) and the depth the
+    library's chooser picks for constant per-draft acceptance."""
+    pol = vb.Policy(**POLICY)
+    rows_ms = {}
+    for R in COST_ROWS:
+        k = R - 1
+        acts = [torch.from_numpy(synth.activations(R, H, 7000 + 10 * R + j)).to(dev) for j in range(8)]
+        rng = np.random.default_rng(R)
+        drafts = [torch.from_numpy(rng.integers(0, V, k).astype(np.int32)).to(dev) if k else None
+                  for _ in range(8)]
+        lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+        o = torch.empty(R, dtype=torch.int32, device=dev)
+        acc = torch.empty(1, dtype=torch.int32, device=dev)
+        ne = torch.empty(1, dtype=torch.int32, device=dev)
+        ws = vb.workspace(R, H, V, device=dev)
+
+        def win(i):
+            vb.verify_window(wd, acts[i % 8], drafts[i % 8], pol, i, 4096, lg, o, acc, ne, ws,
+                             stream=stream)
+        rows_ms[R] = 1000.0 * _event_time(torch, stream, win, 64)
+    rows = list(rows_ms)
+    a, b = vb.cost_fit(rows, [rows_ms[r] for r in rows])
+    choose = {}
+    for alpha in (0.3, 0.5, 0.7, 0.9):
+        k, rate = vb.choose_depth([alpha] * 24, a, b)
+        choose[str(alpha)] = {"k": k, "tokens_per_ms": rate}
+    return {"window_us_by_rows": {str(r): round(1000.0 * t, 2) for r, t in rows_ms.items()},
+            "fit_us": {"one_row": 1000.0 * a, "per_extra_row": 1000.0 * b},
+            "break_even_tokens": {str(r): (a + b * (r - 1)) / a for r in (2, 3, 4, 9, 25)},
+            "chosen_depth_kmax24": choose,
+            "drafts": "point-mass (no candidates), T 0.7, top-k 20, min-p 0.05, top-p 0.95"}
+
+
+TOPK_ROWS, TOPK_VOCAB, TOPK_K = 15, 248320, 16
+
+
+def topk_inputs(torch, dev, n):
+    """n distinct 15 x 248320 float rows with ties, NaN and -inf (seeded)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    xs = []
+    for i in range(n):
+        x = torch.randn((TOPK_ROWS, TOPK_VOCAB), generator=g, device=dev)
+        x = torch.round(x * 64) / 64                       # many exact ties
+        m = torch.rand(x.shape, generator=g, device=dev)
+        x[m < 0.01] = float("nan")
+        x[(m >= 0.01) & (m < 0.02)] = float("-inf")
+        xs.append(x)
+    return xs
+
+
+def topk_workload(torch, vb, dev, stream, n_steps):
+    """The draft tuner's batched top-K: 15 rows x 248320, K 16.  16 distinct
+    inputs (238 MB, above the L2) cycled.  One call is a single ~10 us
+    launch, shorter than the Python binding's own per-call cost, so the 16
+    calls are captured once in a CUDA graph and the graph is replayed; events
+    on the stream.  Also reported: the same calls issued one by one from
+    Python (host-bound)."""
+    xs = topk_inputs(torch, dev, 16)
+    ids = torch.empty((TOPK_ROWS, TOPK_K), dtype=torch.int32, device=dev)
+    vals = torch.empty((TOPK_ROWS, TOPK_K), dtype=torch.float32, device=dev)
+    ws = vb.workspace(TOPK_ROWS, 8, TOPK_VOCAB, device=dev)
+    nbytes = TOPK_ROWS * TOPK_VOCAB * 4
+    t_py = _event_time(torch, stream, lambda i: vb.topk(xs[i % 16], TOPK_K, ids, vals, ws,
+                                                        stream=stream), max(200, n_steps // 10))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(16):                      # warm-up outside the capture
+            vb.topk(xs[i], TOPK_K, ids, vals, ws)
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(16):
+            vb.topk(xs[i], TOPK_K, ids, vals, ws)
+    stream.wait_stream(side)
+    n_rep = max(20, n_steps // 50)
+    t_graph = _event_time(torch, stream, lambda i: g.replay(), n_rep) / 16
+    return {"us_per_call": 1e6 * t_graph, "input_gbs": nbytes / t_graph / 1e9,
+            "us_per_call_python_loop": 1e6 * t_py, "rows": TOPK_ROWS, "vocab": TOPK_VOCAB,
+            "k": TOPK_K, "timing": "CUDA graph of 16 calls on 16 distinct inputs, replayed"}
+
+
+def run_topk_only(torch, vb, dev, args):
+    """Batched top-K (15 x 248320, K 16), warm-up + steps times."""
+    xs = topk_inputs(torch, dev, 2)
+    ids = torch.empty((TOPK_ROWS, TOPK_K), dtype=torch.int32, device=dev)
+    vals = torch.empty((TOPK_ROWS, TOPK_K), dtype=torch.float32, device=dev)
+    ws = vb.workspace(TOPK_ROWS, 8, TOPK_VOCAB, device=dev)
+    for i in range(args.warmup):
+        vb.topk(xs[i % 2], TOPK_K, ids, vals, ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        vb.topk(xs[i % 2], TOPK_K, ids, vals, ws)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"mode": "topk", "steps": args.steps,
+                      "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
 
 
 def run_projection_only(torch, vb, synth, wd, dev, args):
@@ -396,6 +507,9 @@ def main():
     vbuild.build()
     vb.lib()
 
+    if args.mode == "topk":
+        run_topk_only(torch, vb, dev, args)
+        return
     if args.mode == "project_batched":
         run_batched_projection_only(torch, vb, synth, dev, args)
         return
@@ -501,6 +615,7 @@ def main():
 
     extra = None if args.no_extra else extra_workloads(torch, vb, synth, wd, dev, stream,
                                                        min(args.steps, 1000))
+    cost_model = None if args.no_extra else window_cost_model(torch, vb, synth, wd, dev, stream)
 
     # ---- e2e: host inputs -> window -> host outputs, through the C ABI ----
     pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
@@ -547,11 +662,14 @@ def main():
                       "pool_select_only": select_us,
                       "window": 1e6 * job_s / args.steps},
         "rows_sweep_us": sweep,
+        "window_cost_model": cost_model,
         "other_workloads": extra,
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_units / e2e_job_s, "unit": "windows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * args.steps,
+        # per timed window: split_planes, project_tc, sample_rows (no
+        # penalties in this workload, so no penalty or q-copy launches)
+        "gpu_launches": 3 * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = cpu_oracle_windows(W, win, 3)

@@ -183,6 +183,21 @@ VR_API int vr_verify_select(const float* logits, int rows, int vocab, int32_t* p
                      float* pool_vals, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Batched top-K of float rows: the first k entries of each row in the pool
+ * order above (value descending, token id ascending, NaN below -inf, -0.0
+ * below +0.0).  The same select as vr_verify_select cut to k; it serves the
+ * many-row top-K of a draft tuner ("feat(dflash): developer-only online
+ * draft tuning", the re-grid top-K select measured at 15 rows x 248320,
+ * K = 16, gated on byte identity with ties, NaN and -inf).
+ * x [rows][vocab]; ids/vals [rows][k] (row stride k); k in [1, VR_POOL];
+ * slots past min(k, vocab) get id -1 and value NaN; vals holds x's own bits.
+ * rows in [1, VR_MAX_ROWS].  Scratch from ws as for vr_verify_select
+ * (vr_workspace_bytes(rows, 8, vocab) suffices).
+ */
+VR_API int vr_topk(const float* x, int rows, int vocab, int k, int32_t* ids, float* vals,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
  * vr_verify_select without a workspace.  The pages have no counterpart: this
  * entry point exists for callers that cannot give the library device memory
  * of its own (for example a plugin whose host application owns every device
@@ -300,6 +315,78 @@ VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int
                           uint64_t seed, uint64_t position, float* logits, float* pen_logits,
                           int32_t* out_ids_h, int32_t* out_accept_h, int32_t* out_n_emitted_h,
                           void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host-side draft proposal and window pricing.  These run on the CPU, take
+ * HOST pointers only, enqueue nothing and need no GPU.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Prompt-lookup draft proposal ("Speculative decoding on RDNA" §06, N-gram
+ * takeovers: a request-local n-gram pool over the whole context, default
+ * match 5 / propose 3; "One RDNA4 verify pass has slack for about two dozen
+ * speculative tokens", "Spend the budget on a tree": the top few matches
+ * become the branches of one token tree).
+ *   1. key = the last `match` tokens of context[0..len);
+ *   2. every earlier occurrence of key (start s with s + match < len)
+ *      proposes context[s + match .. min(len, s + match + propose));
+ *   3. identical proposals are merged and ranked by how many occurrences
+ *      propose them, then by the most recent occurrence;
+ *   4. the first `branches` proposals are inserted, in rank order, into one
+ *      tree (a trie: a proposal sharing a prefix with an earlier one shares
+ *      its nodes), new nodes appended, stopping at max_nodes nodes.
+ * Out: out_tokens/out_parent [max_nodes] in the window layout above (parent
+ * -1 = the root, every parent an earlier node; branches == 1 gives a chain),
+ * *out_n_nodes (0 when the key has no earlier occurrence or len <= match).
+ * match, propose, branches >= 1; 0 <= max_nodes <= VR_MAX_WINDOW_ROWS - 1.
+ * All pointers are host memory.
+ */
+VR_API int vr_ngram_propose(const int32_t* context, int len, int match, int propose,
+                            int branches, int max_nodes, int32_t* out_tokens,
+                            int32_t* out_parent, int32_t* out_n_nodes);
+
+/*
+ * Window cost model ("Speculative decoding on RDNA" §05: window cost =
+ * one-row cost + a per-row increment for each extra row).  Least-squares fit
+ * of ms[i] = a + b (rows[i] - 1) over n >= 2 measured windows with at least
+ * two distinct row counts.  Host pointers.
+ */
+VR_API int vr_cost_fit(const int32_t* rows, const double* ms, int n, double* out_a,
+                       double* out_b);
+
+/*
+ * Draft depth for the next window (same page, §05): alpha[i] (in [0, 1]) is
+ * the probability that draft i + 1 is accepted once drafts 1..i were;
+ * E(k) = 1 + sum_{j=1..k} prod_{i<=j} alpha_i is the expected number of
+ * emitted tokens with k drafts and a + b k the window's cost.  *out_k is the
+ * k in [0, kmax] with the largest E(k) / (a + b k); k = 0 (one token per
+ * plain step) unless a deeper window is strictly better, and the smaller k
+ * among equal rates.  *out_tokens_per_ms (may be NULL) receives that rate.
+ * a > 0 and a + b kmax > 0.  Host pointers.
+ */
+VR_API int vr_choose_depth(const double* alpha, int kmax, double a, double b, int32_t* out_k,
+                           double* out_tokens_per_ms);
+
+/*
+ * N-gram takeover test (same page, §06): *out_take = 1 iff the n-gram
+ * window's expected emitted tokens per unit of cost, E(alpha_ngram, k_ngram)
+ * / (a + b k_ngram), is at least the native window's at its current
+ * acceptance, E(alpha_native, k_native) / (a + b k_native).  k_ngram >= 1,
+ * k_native >= 0.  Host pointers.
+ */
+VR_API int vr_takeover(const double* alpha_native, int k_native, const double* alpha_ngram,
+                       int k_ngram, double a, double b, int32_t* out_take);
+
+/*
+ * The AR floor's decision (same page, §07): after one timed plain step
+ * (ar_ms) and n timed probe windows (window_ms[i], emitted[i] tokens each),
+ * *out_speculate = 1 iff some probe cost strictly less per emitted token
+ * than the plain step.  A tie, or any invalid timing (not finite, <= 0, or a
+ * probe that emitted nothing), retires the request (*out_speculate = 0).
+ * Host pointers.
+ */
+VR_API int vr_ar_floor(double ar_ms, const double* window_ms, const int32_t* emitted, int n,
+                       int32_t* out_speculate);
 
 /*
  * Read and clear the device status word of a workspace (VR_DEV_* bits).

@@ -99,6 +99,12 @@ _SIGNATURES = {
                             _P, _SZ, _P], _I),
     "vr_verify_select": ([_P, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "vr_verify_select_noalloc": ([_P, _I, _I, _P, _P, _P], _I),
+    "vr_topk": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "vr_ngram_propose": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "vr_cost_fit": ([_P, _P, _I, _P, _P], _I),
+    "vr_choose_depth": ([_P, _I, ctypes.c_double, ctypes.c_double, _P, _P], _I),
+    "vr_takeover": ([_P, _I, _P, _I, ctypes.c_double, ctypes.c_double, _P], _I),
+    "vr_ar_floor": ([ctypes.c_double, _P, _P, _I, _P], _I),
     "vr_verify_policy": ([_P, _I, _I, ctypes.POINTER(vr_policy), _P, _P, _P, _P], _I),
     "vr_verify_sample_accept": ([_P, _I, _I, _P, _P, _I, _P, _P, ctypes.POINTER(vr_policy),
                                  _U64, _U64, _P, _P, _P, _P, _SZ, _P], _I),
@@ -223,6 +229,17 @@ def verify_select(logits, pool_ids, pool_vals, ws, stream=None):
     _check(lib().vr_verify_select(_ptr(logits), R, V, _ptr(pool_ids), _ptr(pool_vals), _ptr(ws),
                                   ws.numel(), _stream(stream, logits.device)), "vr_verify_select")
     return pool_ids, pool_vals
+
+
+def topk(x, k, ids, vals, ws, stream=None):
+    """vr_topk: the first k entries of each row of x in pool order."""
+    R, V = x.shape
+    _dev(x, torch.float32, "x")
+    _dev(ids, torch.int32, "ids", (R, k))
+    _dev(vals, torch.float32, "vals", (R, k))
+    _check(lib().vr_topk(_ptr(x), R, V, k, _ptr(ids), _ptr(vals), _ptr(ws), ws.numel(),
+                         _stream(stream, x.device)), "vr_topk")
+    return ids, vals
 
 
 def verify_select_noalloc(logits, pool_ids, pool_vals, stream=None):
@@ -359,3 +376,69 @@ def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, 
                                        ctypes.byref(acc), ctypes.byref(ne), _ptr(ws), ws.numel(),
                                        _stream(stream, logits.device)), "vr_verify_window_host")
     return acc.value, ne.value
+
+
+# ---------------------------------------------------------------------------
+# host-side draft proposal and window pricing (CPU only, numpy in and out)
+
+def _np(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def ngram_propose(context, match=5, propose=3, branches=1, max_nodes=VR_MAX_WINDOW_ROWS - 1):
+    """vr_ngram_propose: (tokens int32 [n], parent int32 [n]) of the
+    prompt-lookup proposal for the context (prompt || emitted)."""
+    ctx, pctx = _np(context, np.int32)
+    toks = np.zeros(max(1, max_nodes), np.int32)
+    par = np.zeros(max(1, max_nodes), np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib().vr_ngram_propose(pctx if ctx.size else None, ctx.size, match, propose, branches,
+                                  max_nodes, toks.ctypes.data_as(ctypes.c_void_p),
+                                  par.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n)),
+           "vr_ngram_propose")
+    return toks[:n.value].copy(), par[:n.value].copy()
+
+
+def cost_fit(rows, ms):
+    """vr_cost_fit: (a, b) of ms = a + b (rows - 1)."""
+    r, pr = _np(rows, np.int32)
+    m, pm = _np(ms, np.float64)
+    if r.size != m.size:
+        raise ValueError("rows and ms differ in length")
+    a, b = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().vr_cost_fit(pr, pm, r.size, ctypes.byref(a), ctypes.byref(b)), "vr_cost_fit")
+    return a.value, b.value
+
+
+def choose_depth(alpha, a, b, kmax=None):
+    """vr_choose_depth: (k, tokens per unit cost)."""
+    al, pal = _np(alpha, np.float64)
+    kmax = al.size if kmax is None else kmax
+    if kmax > al.size:
+        raise ValueError("alpha needs kmax entries")
+    k = ctypes.c_int32(0)
+    rate = ctypes.c_double(0)
+    _check(lib().vr_choose_depth(pal, kmax, a, b, ctypes.byref(k), ctypes.byref(rate)),
+           "vr_choose_depth")
+    return k.value, rate.value
+
+
+def takeover(alpha_native, alpha_ngram, a, b):
+    """vr_takeover: True if the n-gram window prices at least as well."""
+    an, pan = _np(alpha_native, np.float64)
+    ag, pag = _np(alpha_ngram, np.float64)
+    out = ctypes.c_int32(0)
+    _check(lib().vr_takeover(pan, an.size, pag, ag.size, a, b, ctypes.byref(out)), "vr_takeover")
+    return bool(out.value)
+
+
+def ar_floor(ar_ms, window_ms, emitted):
+    """vr_ar_floor: True to keep speculating, False to retire."""
+    w, pw = _np(window_ms, np.float64)
+    e, pe = _np(emitted, np.int32)
+    if w.size != e.size:
+        raise ValueError("window_ms and emitted differ in length")
+    out = ctypes.c_int32(0)
+    _check(lib().vr_ar_floor(ar_ms, pw, pe, w.size, ctypes.byref(out)), "vr_ar_floor")
+    return bool(out.value)

@@ -1,6 +1,6 @@
 """Build libverifyrow.so in-tree with nvcc for sm_103a.
 
-Each .cu file under csrc/ is compiled to an object in parallel, then linked
+Each .cu and .cpp file under csrc/ is compiled to an object in parallel, then linked
 into one shared library next to this file.  The CUDA runtime is linked
 statically; the driver entry point for tensor maps is looked up at run time,
 so the library loads on a machine without a GPU driver (its entry points
@@ -18,7 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libverifyrow.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
-         "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
+         "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-ffp-contract=off",
+         "--expt-relaxed-constexpr"]
 
 
 def nvcc():
@@ -29,11 +30,12 @@ def nvcc():
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    """CUDA sources (.cu) and host-only sources (.cpp), all through nvcc."""
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _compile(src, verbose):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, "-I", os.path.join(HERE, "..", "include"), "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")

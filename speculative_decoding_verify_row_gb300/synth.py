@@ -152,3 +152,25 @@ def perturb_draft(argmax_rows, k, pos, vocab, seed):
     t = int(rng.integers(vocab - 1))
     d[pos] = t if t < d[pos] else t + 1
     return d
+
+
+def ngram_context(length, vocab, seed, match=5, plants=(2, 1, 1), cont_len=8):
+    """A context for prompt lookup: a Zipf(1.1) token stream whose last
+    `match` tokens also occur earlier, once per entry of `plants` groups;
+    group g plants the key plants[g] times, each followed by the same
+    cont_len random tokens (so group 0's continuation recurs most often).
+    Returns int32 [length]."""
+    rng = np.random.default_rng(seed)
+    ctx = zipf_history(length, vocab, seed)
+    key = ctx[length - match:].copy()
+    conts = [rng.integers(0, vocab, cont_len).astype(np.int32) for _ in plants]
+    span = match + cont_len
+    slots = rng.permutation((length - match - span) // span)[:sum(plants)] * span
+    i = 0
+    for g, times in enumerate(plants):
+        for _ in range(times):
+            s = int(slots[i])
+            ctx[s:s + match] = key
+            ctx[s + match:s + span] = conts[g]
+            i += 1
+    return ctx

@@ -145,9 +145,9 @@ def test_point_mass_drafts_match_one_finite_candidate():
     accepted = rejected = 0
     for trial in range(60):
         n = int(rng.integers(1, 9))
-        pen = (rng.standard_normal((n + 1, V)) * 2).astype(np.float32)
-        top = np.argsort(-pen, axis=1)[:, :4]
-        tokens = np.array([top[j, int(rng.integers(0, 4))] for j in range(n)], np.int32)
+        pen = (rng.standard_normal((n + 1, V)) * 4).astype(np.float32)
+        top = np.argsort(-pen, axis=1)[:, :2]
+        tokens = np.array([top[j, 0 if rng.random() < 0.7 else 1] for j in range(n)], np.int32)
         q_ids = rng.integers(0, V, (n, 8)).astype(np.int32)
         q_ids[:, 0] = tokens
         q_log = np.full((n, 8), -np.inf, np.float32)

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import verify as ov
+from oracle import draft_policy as od, verify as ov
 from speculative_decoding_verify_row_gb300 import binding as vb, synth
 from gpu_common import require_gpu, dev, dev_weight, assert_logits_close, same_bits_f32
 
@@ -327,3 +327,37 @@ def test_host_entry_point_matches_device_entry_point(big_weights_4096):
     assert list(out.numpy()[:n]) == list(win["ids"][:n])
     # no separate penalised buffer was given, so the penalties went in place
     assert torch.equal(logits.view(torch.int32), win["pen"].view(torch.int32))
+
+
+@pytest.mark.parametrize("shape", ["chain", "tree_greedy", "tree_sampled"])
+def test_ngram_drafted_windows_full_size(big_weights_4096, shape):
+    """Drafts from prompt lookup over the request's own context ("Speculative
+    decoding on RDNA" §06: match 5, propose 3, sampled candidates verified
+    against a point-mass q; "Spend the budget on a tree": three matches at
+    depth 8 as one tree).  The oracle's proposal feeds both sides; the
+    library's own proposer must give the same tree."""
+    bw = big_weights_4096
+    V = 151936
+    stats = {}
+    for s in range(3):
+        ctx = synth.ngram_context(2048, V, seed=900 + s)
+        if shape == "chain":
+            toks, par = od.ngram_propose(ctx, 5, 3, 1, 63)
+            pol = ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95, presence=1.5,
+                            window=64)
+        else:
+            toks, par = od.ngram_propose(ctx, 5, 8, 3, 24)
+            pol = ov.Policy(temperature=0.0 if shape == "tree_greedy" else 0.7, top_k=20,
+                            presence=1.5, window=64)
+        lt, lp = vb.ngram_propose(ctx, 5, 3 if shape == "chain" else 8,
+                                  1 if shape == "chain" else 3, 63 if shape == "chain" else 24)
+        assert list(lt) == toks and list(lp) == par
+        tokens = np.array(toks, np.int32)
+        parent = None if shape == "chain" else np.array(par, np.int32)
+        R = len(tokens) + 1
+        A = synth.activations(R, 4096, 900 + s)
+        L64 = bw.oracle_logits(A)
+        win = run_window(bw.dev, A, tokens, pol, s, len(ctx), parent=parent, hist=ctx)
+        check_window(win, L64, tokens, pol, s, len(ctx), parent=parent, hist=ctx, stats=stats,
+                     logit_cols=cols_sample(V, 900 + s))
+    assert stats["compared"] >= 2
