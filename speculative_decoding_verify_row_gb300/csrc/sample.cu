@@ -54,26 +54,37 @@ struct SelectShared {
   int count, gcount, digit, above, n_valid;
 };
 
-constexpr int MERGE_GATHER = 512;
-
 struct MergeShared {
   uint64_t in[MAX_SEG][kPool];
   uint64_t out[MAX_SEG / 2][kPool];
-  uint64_t gather[MERGE_GATHER];
-  uint64_t thr;
-  int count;
+};
+
+constexpr int PT = 64;                       // entries per thread, one-pass segment select
+constexpr int SEG_FAST = THREADS * PT;       // 16384 entries per segment
+constexpr int FAST_CAP = 256;                // entries at or above the threshold, at most
+
+struct FastShared {
+  uint32_t buf[2][THREADS];
+  uint64_t gather[FAST_CAP];
+  uint64_t sorted[kPool];
+  uint32_t warp_cnt[THREADS / 32];
+  uint32_t thr;
 };
 
 union StageShared {
   SelectShared sel;
   MergeShared mrg;
+  FastShared fast;
 };
 
 constexpr int GI_MAX = 20;          // group maxima per thread: vocab <= 32 * 256 * 20
 constexpr int C_MAX = kPool * 32;   // candidates of the chosen groups, at most
 
 struct RowsShared {
-  SelectShared sel;
+  union {
+    SelectShared sel;
+    FastShared fast;
+  };
   uint64_t cands[C_MAX];
   uint64_t pool[kPool];
   int ccount;
@@ -215,6 +226,23 @@ __device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
   __syncthreads();
 }
 
+// cand[0..n) (distinct composites, n <= THREADS) -> sorted[rank] for the
+// ranks below 64 (sorted zeroed by the caller).  Each candidate's rank is
+// counted by q = 4, 2 or 1 threads (as n allows), each over every q-th
+// candidate, and summed by shuffles.
+__device__ __forceinline__ void rank_into(const uint64_t* cand, int n, uint64_t* sorted) {
+  const int tid = threadIdx.x;
+  const int q = n <= THREADS / 4 ? 4 : (n <= THREADS / 2 ? 2 : 1);
+  const int c = tid / q, part = tid % q;
+  const uint64_t me = c < n ? cand[c] : 0ull;
+  int rank = 0;
+  if (c < n)
+    for (int j = part; j < n; j += q) rank += cand[j] > me ? 1 : 0;
+  if (q >= 2) rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+  if (q >= 4) rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+  if (c < n && part == 0 && rank < kPool) sorted[rank] = me;
+}
+
 // Descending bitonic sort of one value per lane across a warp.
 __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
   const int lane = threadIdx.x & 31;
@@ -252,7 +280,7 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
   for (int w = 1; w < THREADS / 32; ++w) thr = sh.warp_thr[w] < thr ? sh.warp_thr[w] : thr;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    const bool pass = x[i] != 0ull && x[i] >= thr;
+    const bool pass = (x[i] != 0ull) & (x[i] >= thr);
     const uint32_t ball = __ballot_sync(0xffffffffu, pass);
     if (ball) {
       int base = 0;
@@ -267,18 +295,127 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
   if (n > GATHER_MAX) return false;
   if (tid < kPool) sh.sorted[tid] = 0ull;
   __syncthreads();
-  if (tid < n) {
-    const uint64_t me = sh.gather[tid];
-    int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (sh.gather[j] > me);
-    if (rank < kPool) sh.sorted[rank] = me;
-  }
+  rank_into(sh.gather, n, sh.sorted);
   __syncthreads();
   return true;
 }
 
+// The float whose order key is k (the inverse of float_key); NaN, whose key
+// is 0 whatever its bits, is read back from the row.
+__device__ __forceinline__ float value_of_key(uint32_t k, const float* row, int32_t id) {
+  if (k == 0u) return row[id];
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __device__ __forceinline__ uint64_t composite_at(const float* row, long long e) {
   return pack_key_id(float_key(row[e]), static_cast<uint32_t>(e));
+}
+
+// Descending bitonic sort of one key per thread across the block: thread t
+// ends with the t-th largest.  Partners within a warp exchange by shuffle;
+// across warps through shared memory, two buffers used in turn so that one
+// barrier per such step suffices.
+__device__ __forceinline__ uint32_t block_sort_desc(uint32_t v, uint32_t (&buf)[2][THREADS]) {
+  const int tid = threadIdx.x;
+  int flip = 0;
+#pragma unroll
+  for (int k = 2; k <= THREADS; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint32_t o;
+      if (j >= 32) {
+        buf[flip][tid] = v;
+        __syncthreads();
+        o = buf[flip][tid ^ j];
+        flip ^= 1;
+      } else {
+        o = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      const bool keep_max = ((tid & k) == 0) == ((tid & j) == 0);
+      v = keep_max ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
+
+// Top 64 of the (key, id) composites the block holds, NI keys per thread,
+// into fs.sorted in pool order (zero-padded).  Entry i of thread t is held
+// iff i * THREADS < len (len = entries - t) and has id id0 + i * THREADS.
+// T = the 64th largest of the 256 per-thread largest keys: 64 threads hold a
+// key >= T, so at least 64 entries do, and the top 64 all have keys >= T.
+// The entries with key >= T (usually about 70) are compacted by a block scan
+// and ranked as composites.  Returns false (after a barrier, nothing
+// written) when more than FAST_CAP entries reach T (many ties at T, or one
+// thread holding most of the top); the caller then takes the radix path.
+template <int NI>
+__device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, FastShared& fs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the thread's largest held key, by a reduction tree (unheld keys are 0)
+  uint32_t m[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) m[i] = i * THREADS < len ? key[i] : 0u;
+#pragma unroll
+  for (int w = 1; w < NI; w <<= 1)
+#pragma unroll
+    for (int i = 0; i + w < NI; i += 2 * w) m[i] = max(m[i], m[i + w]);
+  const uint32_t T = block_sort_desc(m[0], fs.buf);
+  if (tid == kPool - 1) fs.thr = T;
+  __syncthreads();
+  const uint32_t thr = fs.thr;
+  // held entries with key >= thr (bitwise tests: no branches)
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) cnt += ((i * THREADS < len) & (key[i] >= thr)) ? 1u : 0u;
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) fs.warp_cnt[warp] = incl;
+  __syncthreads();
+  uint32_t off = incl - cnt, total = 0;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) {
+    const uint32_t t = fs.warp_cnt[w];
+    off += (w < warp) ? t : 0u;
+    total += t;
+  }
+  if (total > static_cast<uint32_t>(FAST_CAP)) {
+    __syncthreads();
+    return false;
+  }
+  if (cnt) {
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if ((i * THREADS < len) & (key[i] >= thr))
+        fs.gather[off++] = pack_key_id(key[i], id0 + static_cast<uint32_t>(i * THREADS));
+  }
+  if (tid < kPool) fs.sorted[tid] = 0ull;
+  __syncthreads();
+  rank_into(fs.gather, static_cast<int>(total), fs.sorted);
+  __syncthreads();
+  return true;
+}
+
+// Top 64 of one segment [s0, s1) of at most SEG_FAST entries in one pass
+// (keys_top64 on the row's float keys; thread t holds s0 + i * THREADS + t).
+__device__ bool segment_top64_fast(const float* __restrict__ rp, long long s0, long long s1,
+                                   FastShared& fs) {
+  const int tid = threadIdx.x;
+  const int n_seg = static_cast<int>(s1 - s0);
+  // every load is unconditional (entries past the segment read its first
+  // entry and are masked), so all PT loads are in flight together
+  float v[PT];
+#pragma unroll
+  for (int i = 0; i < PT; ++i) {
+    const int e = i * THREADS + tid;
+    v[i] = ld_once(rp + s0 + (e < n_seg ? e : 0));
+  }
+  uint32_t key[PT];
+#pragma unroll
+  for (int i = 0; i < PT; ++i) key[i] = float_key(v[i]);
+  return keys_top64(key, n_seg - tid, static_cast<uint32_t>(s0) + static_cast<uint32_t>(tid), fs);
 }
 
 // ---------------------------------------------------------------------------
@@ -300,60 +437,26 @@ __device__ __forceinline__ uint64_t merged_at(const uint64_t* a, const uint64_t*
 
 // Merge the row's nseg sorted lists (each the top 64 of its segment) into
 // the row's top 64, in pool order.  Returns the list (shared memory).
-//
-// Filter first: with tau the 8th largest of the lists' 8th entries, eight
-// lists hold eight entries each at or above tau, so the top 64 all lie at
-// or above it.  Those entries (usually about a hundred) are compacted and
-// ranked against each other.  If too many pass, the lists are merged
-// pairwise instead (merge path): the top 64 of the union of two lists is the
-// top 64 of their merge, so merging pairs until one list is left gives the
-// pool.
+// Pairwise merge path: the top 64 of the union of two lists is the top 64 of
+// their merge, and each output position is found by a binary search, so
+// ceil(log2(nseg)) rounds of independent searches give the pool.
 __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeShared& ms) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  for (int i = tid; i < nseg * kPool; i += THREADS) ms.in[i / kPool][i % kPool] = lists[i];
-  if (tid == 0) ms.count = 0;
-  __syncthreads();
-  if (nseg == 1) return ms.in[0];
-  if (tid < nseg) {
-    const uint64_t me = ms.in[tid][7];
-    int rank = 0;
-    for (int s = 0; s < nseg; ++s) {
-      const uint64_t o = ms.in[s][7];
-      rank += (o > me) || (o == me && s < tid);
+  const int tid = threadIdx.x;
+  const int total = nseg * kPool;
+  for (int base = 0; base < total; base += 4 * THREADS) {
+    uint64_t t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * THREADS + tid;
+      t[u] = lists[i < total ? i : 0];               // unconditional: loads overlap
     }
-    if (rank == 7) ms.thr = me;
-  }
-  if (nseg < 8 && tid == 0) ms.thr = 1ull;       // fewer than 8 lists: take every entry
-  __syncthreads();
-  const uint64_t thr = ms.thr;
-  for (int base = 0; base < nseg * kPool; base += THREADS) {
-    const int i = base + tid;
-    const uint64_t v = i < nseg * kPool ? ms.in[i / kPool][i % kPool] : 0ull;
-    const bool pass = v != 0ull && v >= thr;
-    const uint32_t ball = __ballot_sync(0xffffffffu, pass);
-    if (ball) {
-      int at = 0;
-      if (lane == 0) at = atomicAdd(&ms.count, __popc(ball));
-      at = __shfl_sync(0xffffffffu, at, 0);
-      const int pos = at + __popc(ball & ((1u << lane) - 1u));
-      if (pass && pos < MERGE_GATHER) ms.gather[pos] = v;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * THREADS + tid;
+      if (i < total) ms.in[i / kPool][i % kPool] = t[u];
     }
   }
   __syncthreads();
-  const int n = ms.count;
-  if (n <= MERGE_GATHER) {
-    uint64_t* out = ms.out[0];
-    if (tid < kPool) out[tid] = 0ull;
-    __syncthreads();
-    for (int t = tid; t < n; t += THREADS) {
-      const uint64_t me = ms.gather[t];
-      int rank = 0;
-      for (int j = 0; j < n; ++j) rank += (ms.gather[j] > me);
-      if (rank < kPool) out[rank] = me;
-    }
-    __syncthreads();
-    return out;
-  }
   uint64_t(*src)[kPool] = ms.in;
   uint64_t(*dst)[kPool] = ms.out;
   int nl = nseg;
@@ -635,7 +738,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
     float v = __int_as_float(0x7fffffff);
     if (tid < n) {
       id = static_cast<int32_t>(packed_id(pool[tid]));
-      v = rp[id];
+      v = value_of_key(static_cast<uint32_t>(pool[tid] >> 32), rp, id);
     }
     if (tid < a.out_k) {
       a.pool_ids[static_cast<size_t>(row) * a.out_k + tid] = id;
@@ -666,7 +769,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
 // the kernel
 
 
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 2)
     sample_kernel(SampleArgs a, ReqTable tab) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   StageShared& st = *reinterpret_cast<StageShared*>(dyn_smem);
@@ -678,18 +781,31 @@ __global__ void __launch_bounds__(THREADS)
   const int seg = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
 
-  // 1. the segment's top 64, stored in pool order
+  // 1. the segment's top 64, stored in pool order: in one pass when the
+  // segment fits the registers (the usual case), else sub-block by sub-block
   {
     SelectShared& sh = st.sel;
     const long long s0 = static_cast<long long>(seg) * a.seg_len;
     const long long s1 = std::min<long long>(s0 + a.seg_len, a.vocab);
     uint64_t carry = 0ull;            // thread t < 64: entry t of the running list
-    for (long long b = s0; b < s1; b += SUB) {
+    long long from = s0;
+    if (a.seg_len == SEG_FAST && segment_top64_fast(rp, s0, s1, st.fast)) {
+      carry = tid < kPool ? st.fast.sorted[tid] : 0ull;
+      from = s1;
+      __syncthreads();
+    }
+    for (long long b = from; b < s1; b += SUB) {
       uint64_t x[ITEMS];
+      float f[SUB / THREADS];
 #pragma unroll
       for (int i = 0; i < SUB / THREADS; ++i) {
         const long long e = b + i * THREADS + tid;
-        x[i] = (e < s1) ? composite_at(rp, e) : 0ull;
+        f[i] = __ldg(rp + (e < s1 ? e : b));          // unconditional: loads overlap
+      }
+#pragma unroll
+      for (int i = 0; i < SUB / THREADS; ++i) {
+        const long long e = b + i * THREADS + tid;
+        x[i] = (e < s1) ? pack_key_id(float_key(f[i]), static_cast<uint32_t>(e)) : 0ull;
       }
       x[ITEMS - 1] = carry;
       if (!block_top64_filtered(x, sh)) {
@@ -739,32 +855,51 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
 
   // (a) top 64 groups, as composites (max key << 32) | ~group
+  const uint64_t* chosen = sr.fast.sorted;
   {
-    uint64_t x[GI_MAX];
+    uint32_t gk[GI_MAX];
 #pragma unroll
     for (int i = 0; i < GI_MAX; ++i) {
       const int g = i * THREADS + tid;
-      x[i] = g < ngroups ? pack_key_id(gm[g], static_cast<uint32_t>(g)) : 0ull;
+      gk[i] = __ldg(gm + (g < ngroups ? g : 0));      // unconditional: loads overlap
     }
-    if (!block_top64_filtered(x, sh)) {
+    if (!keys_top64(gk, ngroups - tid, static_cast<uint32_t>(tid), sr.fast)) {
+      uint64_t x[GI_MAX];
+#pragma unroll
+      for (int i = 0; i < GI_MAX; ++i) {
+        const int g = i * THREADS + tid;
+        x[i] = g < ngroups ? pack_key_id(gk[i], static_cast<uint32_t>(g)) : 0ull;
+      }
       block_top64(x, sh);
       sort_out_into_sorted(sh);
+      chosen = sh.sorted;
     }
   }
   const int nchosen = ngroups < kPool ? ngroups : kPool;
-  const uint32_t tau = static_cast<uint32_t>(sh.sorted[nchosen - 1] >> 32);
+  const uint32_t tau = static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
   if (tid == 0) sr.ccount = 0;
   __syncthreads();
 
-  // (b) the chosen groups' entries at or above tau; a warp per group
-  for (int j = warp; j < nchosen; j += THREADS / 32) {
-    const uint32_t g = packed_id(sh.sorted[j]);
-    const long long v = static_cast<long long>(g) * 32 + lane;
+  // (b) the chosen groups' entries at or above tau; warp w takes groups
+  // w, w + 8, ...: all of its loads are issued before any is used
+  constexpr int GPW = kPool / (THREADS / 32);     // groups per warp
+  float fv[GPW];
+#pragma unroll
+  for (int t = 0; t < GPW; ++t) {
+    const int j = warp + t * (THREADS / 32);
+    const long long v = static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
+    fv[t] = __ldg(rp + (v < a.vocab ? v : 0));        // unconditional: loads overlap
+  }
+  uint32_t kv[GPW];
+#pragma unroll
+  for (int t = 0; t < GPW; ++t) kv[t] = float_key(fv[t]);
+#pragma unroll
+  for (int t = 0; t < GPW; ++t) {
+    const int j = warp + t * (THREADS / 32);
+    if (j >= nchosen) break;
+    const long long v = static_cast<long long>(packed_id(chosen[j])) * 32 + lane;
     uint64_t c = 0ull;
-    if (v < a.vocab) {
-      const uint32_t k = float_key(rp[v]);
-      if (k >= tau) c = pack_key_id(k, static_cast<uint32_t>(v));
-    }
+    if (v < a.vocab && kv[t] >= tau) c = pack_key_id(kv[t], static_cast<uint32_t>(v));
     const uint32_t ball = __ballot_sync(0xffffffffu, c != 0ull);
     if (ball) {
       int at = 0;
@@ -781,12 +916,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (n <= GATHER_MAX) {
     if (tid < kPool) pool[tid] = 0ull;
     __syncthreads();
-    if (tid < n) {
-      const uint64_t me = sr.cands[tid];
-      int rank = 0;
-      for (int j = 0; j < n; ++j) rank += (sr.cands[j] > me);
-      if (rank < kPool) pool[rank] = me;
-    }
+    rank_into(sr.cands, n, pool);
     __syncthreads();
   } else {
     uint64_t x[C_MAX / THREADS];
@@ -826,10 +956,22 @@ __global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len,
 
 }  // namespace smp
 
+namespace {
+
+// Segment length of a row: SEG_FAST (one pass in registers) while the row
+// needs at most MAX_SEG such segments, else the smallest multiple of SUB
+// that keeps the row within MAX_SEG segments.
+long long segment_length(int vocab) {
+  if (static_cast<long long>(vocab) <= static_cast<long long>(smp::MAX_SEG) * smp::SEG_FAST)
+    return smp::SEG_FAST;
+  const long long per = (static_cast<long long>(vocab) + smp::MAX_SEG - 1) / smp::MAX_SEG;
+  return (per + smp::SUB - 1) / smp::SUB * smp::SUB;
+}
+
+}  // namespace
+
 int select_segments(int vocab) {
-  int nseg = std::min((vocab + smp::SUB - 1) / smp::SUB, smp::MAX_SEG);
-  const long long per = (static_cast<long long>(vocab) + nseg - 1) / nseg;
-  const long long seg_len = (per + smp::SUB - 1) / smp::SUB * smp::SUB;
+  const long long seg_len = segment_length(vocab);
   return static_cast<int>((vocab + seg_len - 1) / seg_len);
 }
 
@@ -842,11 +984,10 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
                   int4* dec, int32_t* status, cudaStream_t stream, int out_k) {
   if (out_k < 1 || out_k > kPool) return VR_ERR_ARG;
   const int nseg = select_segments(vocab);
-  const long long per = (static_cast<long long>(vocab) + nseg - 1) / nseg;
   smp::SampleArgs a;
   a.logits = logits;
   a.vocab = vocab;
-  a.seg_len = static_cast<int>((per + smp::SUB - 1) / smp::SUB * smp::SUB);
+  a.seg_len = static_cast<int>(segment_length(vocab));
   a.nseg = nseg;
   a.cand = cand;
   a.row_ticket = row_ticket;

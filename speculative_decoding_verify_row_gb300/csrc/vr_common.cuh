@@ -71,6 +71,16 @@ __device__ __forceinline__ bool penalties_active(const vr_policy& p) {
 // total order of float32 used by the pool: unsigned order of the key below
 // is value order with every NaN lowest and -0.0 below +0.0.
 
+// A float read the compiler must keep: the asm is volatile, so the load is
+// issued once where written and its value held in a register, never dropped
+// and re-read later under register pressure (which a plain read-only load
+// may be).  Read-only path, no L1 allocation: the data is read once.
+__device__ __forceinline__ float ld_once(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t float_key(float x) {
   const uint32_t b = __float_as_uint(x);
   if (isnan(x)) return 0u;
