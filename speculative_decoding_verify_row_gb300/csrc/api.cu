@@ -35,7 +35,7 @@ Layout layout(int rows, int hidden, int vocab) {
   };
   const size_t r = static_cast<size_t>(rows);
   L.status = take(kControlBytes);
-  L.planes = take(std::max(tc_plane_bytes(rows, hidden), tcb_plane_bytes(rows, hidden)));
+  L.planes = take(std::max(tcb_plane_bytes(rows, hidden), tc_scratch_bytes(rows, hidden)));
   L.cand = take(select_cand_bytes(rows, vocab));
   L.gmax = take(r * ((static_cast<size_t>(vocab) + 31) / 32) * 4);
   L.pool_ids = take(r * kPool * 4);

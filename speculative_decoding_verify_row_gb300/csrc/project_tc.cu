@@ -15,11 +15,18 @@
 //    N = 96, K = 16) and the same K order whatever the row count: rows past
 //    R are zero columns.  Row r's bits therefore do not depend on R.
 //  * Each CTA (one per SM, persistent) walks units of two 128-row vocab
-//    tiles.  Warp 0 streams W tiles (2 x 16 KB) and the shared plane tile
-//    (12 KB) per 64-wide K block through a 5-stage TMA ring; one thread of
-//    warp 1 issues the MMAs into a double-buffered TMEM accumulator
-//    (2 x 192 columns); warps 2-5 drain TMEM and write the logits, so the
-//    epilogue of one unit overlaps the weight stream of the next.
+//    tiles.  Per 64-wide K block, one thread of warp 0 streams the two W
+//    tiles (2 x 16 KB) through a 5-stage TMA ring together with the block's
+//    plane tile (96 x 64 bf16, in the 128-byte swizzled layout the MMA
+//    reads).  For up to 16 rows the planes are built in the kernel: the TMA
+//    brings the group's fp32 activations for the block (R x 64) into the
+//    end of the plane tile and warp 6 splits them in place, so no separate
+//    pass runs before the projection.  For more rows one warp cannot keep
+//    pace with the weight stream, so a split kernel writes the planes of
+//    every group first and the TMA loads plane tiles.  One thread of warp 1
+//    issues the MMAs into a double-buffered TMEM accumulator (2 x 192
+//    columns); warps 2-5 drain TMEM and write the logits, so the epilogue of
+//    one unit overlaps the weight stream of the next.
 //  * Optionally the epilogue also records, per row and per 32 vocabulary
 //    rows, the largest order key (a warp max), which lets the sampling stage
 //    find a row's top 64 without reading the whole row.
@@ -50,7 +57,9 @@ constexpr int B_TILE_BYTES = BN * BK * 2;            // 12288
 constexpr int STAGE_BYTES = MT * W_TILE_BYTES + B_TILE_BYTES;
 constexpr int TMEM_COLS_PER_BUF = MT * BN;           // 192
 constexpr int TMEM_ALLOC = 512;
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;              // 7 warps: TMA, MMA, 4 x epilogue, planes
+constexpr int PLANE_WARP = 6;
+constexpr int FUSED_MAX_ROWS = 16;        // planes built in the kernel up to this many rows
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -61,17 +70,127 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
 
 using namespace tcx;
 
+// (lo, hi) rounded to bf16 (nearest, ties to even) and packed, lo in the low
+// half: one conversion instruction for two values.
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 x) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(x.x, x.y);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// the two bf16 of a packed pair as floats (exact)
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t p) {
+  return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+}
+
+// Plane tiles, built in the kernel (groups of at most 16 rows).  The TMA
+// lands the group's activations for one K block, act[row_base + r][kb*64 ..
+// + 64) for r < R (zeros past hidden), as R rows of 256 bytes at the end of
+// the stage's 12 KB plane tile.  Warp 6 then writes, for the group's rows
+// r < R and 16-byte chunks j of the block, hi/mid/lo of those 8 values into
+// rows p*32 + r (p = 0, 1, 2) of the tile, chunk j at chunk position
+// j ^ (row & 7) of its 128-byte row (the 128-byte swizzle); hi = RN(a),
+// mid = RN(a - hi), lo = RN(a - hi - mid), all exact.  Work item
+// i = lane + 32 t is (r, j) = (i / 8, i % 8); NIT items per lane.
+template <int NIT>
+__device__ __forceinline__ void split_block(uint8_t* btile, int rows_in_group, int lane) {
+  const int n_items = rows_in_group * (BK / 8);
+  const int stg_off = B_TILE_BYTES - rows_in_group * BK * 4;
+  const float* stg = reinterpret_cast<const float*>(btile + stg_off);
+  float a[NIT][8];
+#pragma unroll
+  for (int t = 0; t < NIT; ++t) {
+    const int it = lane + 32 * t;
+    const int off = it < n_items ? (it >> 3) * BK + (it & 7) * 8 : 0;
+    const float4 x0 = *reinterpret_cast<const float4*>(stg + off);
+    const float4 x1 = *reinterpret_cast<const float4*>(stg + off + 4);
+    a[t][0] = x0.x; a[t][1] = x0.y; a[t][2] = x0.z; a[t][3] = x0.w;
+    a[t][4] = x1.x; a[t][5] = x1.y; a[t][6] = x1.z; a[t][7] = x1.w;
+  }
+  __syncwarp();      // every lane has read the staged block before any write
+  // the staging area, except the group's own plane rows, back to zero
+  for (int off = stg_off + lane * 16; off < B_TILE_BYTES; off += 32 * 16)
+    if (((off >> 7) & (NP - 1)) >= rows_in_group)
+      *reinterpret_cast<uint4*>(btile + off) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int t = 0; t < NIT; ++t) {
+    const int it = lane + 32 * t;
+    if (it >= n_items) continue;
+    const int r = it >> 3, j = it & 7;
+    // pairs of elements, element 2i in the low half; the differences are
+    // exact, so the fused multiply-add by -1 is a plain exact subtraction
+    uint32_t h[4], m[4], l[4];
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float2 x = make_float2(a[t][e], a[t][e + 1]);
+      h[e >> 1] = bf16x2_rn(x);
+      const float2 r1 = __ffma2_rn(bf16x2_to_float2(h[e >> 1]), neg1, x);
+      m[e >> 1] = bf16x2_rn(r1);
+      const float2 r2 = __ffma2_rn(bf16x2_to_float2(m[e >> 1]), neg1, r1);
+      l[e >> 1] = bf16x2_rn(r2);
+    }
+    const int chunk = (j ^ (r & 7)) * 16;
+    *reinterpret_cast<uint4*>(btile + (0 * NP + r) * 128 + chunk) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(btile + (1 * NP + r) * 128 + chunk) = make_uint4(m[0], m[1], m[2], m[3]);
+    *reinterpret_cast<uint4*>(btile + (2 * NP + r) * 128 + chunk) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// Groups of more than 16 rows: A [R][H] fp32 -> planes [G][96][H] bf16 in
+// global memory, plane p of row r of group g at plane-row p * 32 + (r - 32 g),
+// rows past R zero; the same hi/mid/lo split.
+__global__ void split_planes_kernel(const float* __restrict__ act, int rows, int hidden,
+                                    int groups, __nv_bfloat16* __restrict__ planes) {
+  pdl_trigger();
+  pdl_wait();
+  const int chunks = hidden / 8;
+  const long long total = static_cast<long long>(groups) * NP * chunks;
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % chunks);
+    const int r = static_cast<int>(i / chunks);        // global row (g * 32 + local row)
+    const int g = r / NP, rl = r % NP;
+    float a[8];
+    const float* src = act + static_cast<size_t>(r < rows ? r : 0) * hidden + c * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = r < rows ? src[j] : 0.0f;
+    uint32_t h[4], m[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float2 x = make_float2(a[e], a[e + 1]);
+      h[e >> 1] = bf16x2_rn(x);
+      const float2 r1 = __ffma2_rn(bf16x2_to_float2(h[e >> 1]), neg1, x);
+      m[e >> 1] = bf16x2_rn(r1);
+      const float2 r2 = __ffma2_rn(bf16x2_to_float2(m[e >> 1]), neg1, r1);
+      l[e >> 1] = bf16x2_rn(r2);
+    }
+    const size_t base = (static_cast<size_t>(g) * BN + rl) * hidden + c * 8;
+    *reinterpret_cast<uint4*>(planes + base) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(planes + base + static_cast<size_t>(NP) * hidden) =
+        make_uint4(m[0], m[1], m[2], m[3]);
+    *reinterpret_cast<uint4*>(planes + base + static_cast<size_t>(2 * NP) * hidden) =
+        make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// NIT > 0: planes built in the kernel (tm_x: the fp32 activations, boxes of
+// 64 x R); NIT == 0: plane tiles loaded (tm_x: the bf16 planes of this
+// group, boxes of 64 x 96, 128-byte swizzle).
+template <int NIT>
 __global__ void __launch_bounds__(THREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
-                      const __grid_constant__ CUtensorMap tm_b, int hidden, int vocab,
+                      const __grid_constant__ CUtensorMap tm_x, int hidden, int vocab,
                       int rows_in_group, int row_base, float* __restrict__ logits,
                       uint32_t* __restrict__ gmax, int ngroups, int32_t* status) {
+  constexpr bool kFused = NIT > 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2],
+  // act_full[STAGES]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -84,11 +203,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  auto afull_bar = [&](int s) { return smem_u32(bars + 2 * STAGES + 4 + s); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      // the bytes' arrive.expect_tx, and the plane warp's arrival when it
+      // builds the planes
+      mbar_init(full_bar(s), kFused ? 2 : 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(afull_bar(s), 1);      // the staged activations
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -100,7 +223,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+  }
+  if (kFused && warp == PLANE_WARP) {
+    // zero every stage's plane tile once (private shared memory, so before
+    // the wait below): rows past the group are never written again
+    for (int s = 0; s < STAGES; ++s) {
+      uint4* t = reinterpret_cast<uint4*>(smem + s * STAGE_BYTES + MT * W_TILE_BYTES);
+      for (int i = lane; i < B_TILE_BYTES / 16; i += 32) t[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // ordered before the bulk copies that later land in these tiles
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -113,8 +246,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // the prologue above overlaps the previous kernel; from here on the planes
-  // and the logits buffer are touched, so wait for it to complete
+  // the prologue above overlaps the previous kernel; from here on the
+  // activations and the logits buffer are touched, so wait for it to complete
   pdl_trigger();
   pdl_wait();
 
@@ -122,22 +255,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- producer: TMA ring ----------------
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_last();
+      const uint64_t pol_x = l2_policy_evict_last();     // shared by every CTA
+      const uint32_t a_bytes = static_cast<uint32_t>(rows_in_group) * BK * 4;
+      const int stg_off = B_TILE_BYTES - rows_in_group * BK * 4;
       int s = 0;
       uint32_t ph = 0;
       int last_fill_parity[STAGES];
       for (int i = 0; i < STAGES; ++i) last_fill_parity[i] = -1;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
         const int nmt = min(MT, n_mtiles - u * MT);
-        const uint32_t bytes = nmt * W_TILE_BYTES + B_TILE_BYTES;
+        const uint32_t bytes = nmt * W_TILE_BYTES + (kFused ? 0 : B_TILE_BYTES);
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) break;
-          mbar_expect_tx(full_bar(s), bytes);
           uint8_t* st = smem + s * STAGE_BYTES;
+          if (kFused) {
+            mbar_expect_tx(afull_bar(s), a_bytes);
+            tma_load_2d(smem_u32(st + MT * W_TILE_BYTES + stg_off), &tm_x, kb * BK, row_base,
+                        afull_bar(s), pol_x);
+          }
+          mbar_expect_tx(full_bar(s), bytes);
+          if (!kFused)
+            tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_x, kb * BK, 0, full_bar(s), pol_x);
           for (int mt = 0; mt < nmt; ++mt)
             tma_load_2d(smem_u32(st + mt * W_TILE_BYTES), &tm_w, kb * BK, (u * MT + mt) * BM,
                         full_bar(s), pol_w);
-          tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_b, kb * BK, 0, full_bar(s), pol_b);
           last_fill_parity[s] = static_cast<int>(ph);
           if (++s == STAGES) {
             s = 0;
@@ -151,6 +292,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < STAGES; ++i) {
           if (last_fill_parity[i] < 0) continue;
           const long long t0 = clock64();
+          while (kFused &&
+                 !mbar_try_wait(afull_bar(i), static_cast<uint32_t>(last_fill_parity[i])) &&
+                 clock64() - t0 < kWaitLimitCycles / 8) {
+          }
           while (!mbar_try_wait(full_bar(i), static_cast<uint32_t>(last_fill_parity[i])) &&
                  clock64() - t0 < kWaitLimitCycles / 8) {
           }
@@ -205,6 +350,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         const long long t0 = clock64();
         while (!mbar_try_wait(tfull_bar(buf), bph) && clock64() - t0 < kWaitLimitCycles / 8) {
         }
+      }
+    }
+  } else if (warp == PLANE_WARP) {
+    // ---------------- planes: activations -> swizzled bf16 plane tiles ----------------
+    if constexpr (kFused) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        bool ok = true;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          ok = mbar_wait(afull_bar(s), ph, abort_flag, status);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          split_block<NIT>(smem + s * STAGE_BYTES + MT * W_TILE_BYTES, rows_in_group, lane);
+          // generic-proxy writes, read by the MMA (async proxy) after the barrier
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
     }
   } else {
@@ -263,42 +432,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// A [R][H] fp32 -> planes [G][96][H] bf16: plane p of row r of group g sits
-// at plane-row p * 32 + (r - 32 g); rows past R are zero.  hi = RN(a),
-// mid = RN(a - hi), lo = RN(a - hi - mid); both subtractions are exact.
-__global__ void split_planes_kernel(const float* __restrict__ act, int rows, int hidden,
-                                    int groups, __nv_bfloat16* __restrict__ planes) {
-  pdl_trigger();
-  pdl_wait();
-  const int chunks = hidden / 8;
-  const long long total = static_cast<long long>(groups) * NP * chunks;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(i % chunks);
-    const int rr = static_cast<int>(i / chunks);       // g * 32 + local row
-    const int g = rr / NP, rl = rr % NP;
-    const int r = rr;                                  // global row
-    __align__(16) __nv_bfloat16 h[8], m[8], l[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float a = (r < rows) ? act[static_cast<size_t>(r) * hidden + c * 8 + j] : 0.f;
-      const __nv_bfloat16 bh = __float2bfloat16_rn(a);
-      const float r1 = __fsub_rn(a, __bfloat162float(bh));
-      const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
-      const float r2 = __fsub_rn(r1, __bfloat162float(bm));
-      h[j] = bh;
-      m[j] = bm;
-      l[j] = __float2bfloat16_rn(r2);
-    }
-    const size_t base = (static_cast<size_t>(g) * BN + rl) * hidden + c * 8;
-    *reinterpret_cast<uint4*>(planes + base) = *reinterpret_cast<const uint4*>(h);
-    *reinterpret_cast<uint4*>(planes + base + static_cast<size_t>(NP) * hidden) =
-        *reinterpret_cast<const uint4*>(m);
-    *reinterpret_cast<uint4*>(planes + base + static_cast<size_t>(2 * NP) * hidden) =
-        *reinterpret_cast<const uint4*>(l);
-  }
-}
-
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
@@ -320,7 +453,6 @@ bool get_encoder() {
 }
 
 int g_num_sms = 0;
-bool g_attr_set = false;
 }  // namespace
 
 // 2-D bf16 tensor map over a row-major [outer][inner] array, tiles of
@@ -338,13 +470,50 @@ bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t tc_plane_bytes(int rows, int hidden) {
-  const int groups = (rows + tc::NP - 1) / tc::NP;
-  return static_cast<size_t>(groups) * tc::BN * hidden * 2;
+// 2-D fp32 tensor map over a row-major [outer][inner] array, tiles of
+// box_outer x box_inner elements, no swizzle; reads past the array are zero.
+bool encode_f32_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint32_t box_inner, uint32_t box_outer) {
+  if (!get_encoder()) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+template <int NIT>
+cudaError_t launch_group(const CUtensorMap& tm_w, const CUtensorMap& tm_x, int hidden, int vocab,
+                         int rg, int row_base, float* logits, uint32_t* gmax, int32_t* status,
+                         int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        tc::project_tc_kernel<NIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(tc::project_tc_kernel<NIT>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES,
+                    stream, tm_w, tm_x, hidden, vocab, rg, row_base, logits, gmax,
+                    (vocab + 31) / 32, status);
+}
+
+}  // namespace
+
+size_t tc_scratch_bytes(int rows, int hidden) {
+  const size_t r = static_cast<size_t>(rows), h = static_cast<size_t>(hidden);
+  if (rows <= tc::FUSED_MAX_ROWS) return r * h * sizeof(float);     // an aligned copy of act
+  const size_t groups = (r + tc::NP - 1) / tc::NP;
+  return groups * tc::BN * h * 2;                                   // the planes
 }
 
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                      float* logits, void* planes, uint32_t* gmax, int32_t* status,
+                      float* logits, void* scratch, uint32_t* gmax, int32_t* status,
                       cudaStream_t stream) {
   if (!g_num_sms) {
     int dev = 0;
@@ -352,14 +521,39 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
     if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VR_ERR_CUDA;
   }
-  if (!g_attr_set) {
-    if (cudaFuncSetAttribute(tc::project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::SMEM_BYTES) != cudaSuccess)
-      return VR_ERR_CUDA;
-    g_attr_set = true;
+  CUtensorMap tm_w;
+  if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
+  const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
+  const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
+  const int grid = std::min(n_units, g_num_sms);
+
+  if (rows <= tc::FUSED_MAX_ROWS) {
+    // one group, planes built in the kernel from the activations
+    if (reinterpret_cast<uintptr_t>(act) % 16) {
+      // a tensor map needs a 16-byte aligned base: stage the rows in scratch
+      if (cudaMemcpyAsync(scratch, act, static_cast<size_t>(rows) * hidden * sizeof(float),
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return VR_ERR_CUDA;
+      act = static_cast<const float*>(scratch);
+    }
+    CUtensorMap tm_a;
+    if (!encode_f32_rows(&tm_a, act, hidden, rows, tc::BK, rows)) return VR_ERR_ARG;
+    // plane items per lane of the plane warp: rows x 8 chunks over 32 lanes
+    const int nit = (rows * (tc::BK / 8) + 31) / 32;
+    cudaError_t e;
+    if (nit <= 1)
+      e = launch_group<1>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+    else if (nit <= 2)
+      e = launch_group<2>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+    else
+      e = launch_group<4>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+    if (e != cudaSuccess) return VR_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;
   }
+
+  // groups of 32 rows, planes written by the split kernel first
   const int groups = (rows + tc::NP - 1) / tc::NP;
-  auto* pl = static_cast<__nv_bfloat16*>(planes);
+  auto* pl = static_cast<__nv_bfloat16*>(scratch);
   {
     const long long work = static_cast<long long>(groups) * tc::NP * (hidden / 8);
     const int threads = 256;
@@ -369,20 +563,14 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
                    hidden, groups, pl) != cudaSuccess)
       return VR_ERR_CUDA;
   }
-  CUtensorMap tm_w;
-  if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
-  const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
-  const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
-  const int grid = std::min(n_units, g_num_sms);
   for (int g = 0; g < groups; ++g) {
     CUtensorMap tm_b;
     if (!encode_bf16_tile(&tm_b, pl + static_cast<size_t>(g) * tc::BN * hidden, hidden, tc::BN,
                           tc::BK, tc::BN))
       return VR_ERR_ARG;
     const int rg = std::min(tc::NP, rows - g * tc::NP);
-    if (launch_pdl(tc::project_tc_kernel, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES, stream,
-                   tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, gmax,
-                   (vocab + 31) / 32, status) != cudaSuccess)
+    if (launch_group<0>(tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, gmax, status, grid,
+                        stream) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;

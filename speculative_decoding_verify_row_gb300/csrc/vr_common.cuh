@@ -81,6 +81,13 @@ __device__ __forceinline__ float ld_once(const float* p) {
   return v;
 }
 
+// The same for data read again soon (allocated in L1).
+__device__ __forceinline__ float ld_once_l1(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t float_key(float x) {
   const uint32_t b = __float_as_uint(x);
   if (isnan(x)) return 0u;

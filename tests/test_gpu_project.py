@@ -94,3 +94,27 @@ def test_row_bits_across_row_groups(path):
     for r in (0, 31, 32, 255, 256, 299):
         alone = project(W, A[r:r + 1], path).cpu().numpy().view(np.uint32)
         assert np.array_equal(alone[0], full[r]), r
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_unaligned_activations(path):
+    """Activations at an address that is not 16-byte aligned give the same
+    bits as an aligned copy."""
+    rng = np.random.default_rng(17)
+    V, H, R = 2000, 520, 5
+    Wb = synth.f32_to_bf16_bits(rng.standard_normal((V, H), dtype=np.float32) * np.float32(0.05))
+    W = dev_weight(Wb)
+    A = rng.standard_normal((R, H), dtype=np.float32)
+    aligned = torch.from_numpy(A).cuda()
+    buf = torch.empty(R * H + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = aligned.reshape(-1)
+    shifted = buf[1:].view(R, H)
+    assert shifted.data_ptr() % 16 != 0
+    outs = []
+    for act in (aligned, shifted):
+        lg = torch.empty((R, V), dtype=torch.float32, device="cuda")
+        vb.verify_project(W, act, lg, vb.workspace(R, H, V), path=path)
+        torch.cuda.synchronize()
+        outs.append(lg.cpu().numpy().view(np.uint32))
+    assert np.array_equal(outs[0], outs[1])
+    assert_logits_close(outs[1].view(np.float32), ov.project(Wb, A))
