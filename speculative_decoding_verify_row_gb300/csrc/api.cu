@@ -168,7 +168,8 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
   if (gmax)
     return launch_sample_rows(target, rows, vocab, gmax, at<uint32_t>(ws, L.status + kReqTicketOff),
                               at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
-                              at<int4>(ws, L.dec), at<int32_t>(ws, L.status), s);
+                              at<int4>(ws, L.dec), at<int32_t>(ws, L.status),
+                              any_active && any_q, s);
   return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
                        at<uint32_t>(ws, L.status + kReqTicketOff), at<int32_t>(ws, L.pool_ids),

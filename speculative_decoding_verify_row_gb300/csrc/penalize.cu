@@ -21,7 +21,7 @@ namespace pen {
 constexpr int THREADS = 128;
 
 __global__ void __launch_bounds__(THREADS)
-    penalize_kernel(ReqTable tab, int rows_total, float* __restrict__ logits, int vocab,
+    penalize_kernel(const __grid_constant__ ReqTable tab, int rows_total, float* __restrict__ logits, int vocab,
                     int with_q, uint32_t* __restrict__ gmax, int32_t* status) {
   __shared__ int32_t H[VR_MAX_PENALTY_WINDOW];
   __shared__ int32_t path[VR_MAX_WINDOW_ROWS];
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(THREADS)
           if (i < j) first = false;
         }
       }
-      if (first && t >= 0 && t < vocab) row[t] = penalize_value(row[t], count, pol);
+      if (first && t >= 0 && t < vocab) row[t] = penalize_value(__ldcg(row + t), count, pol);
     }
     if (gmax) {
       // refresh the largest order key of every 32-row group a penalty touched
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(THREADS)
         if (!first) continue;
         uint32_t k = 0u;
         for (int v = g * 32; v < g * 32 + 32 && v < vocab; ++v) {
-          const uint32_t kv = float_key(row[v]);
+          const uint32_t kv = float_key(__ldcg(row + v));
           k = kv > k ? kv : k;
         }
         gmax[static_cast<size_t>(g_row) * ngroups + g] = k;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(THREADS)
       const int t = ids[threadIdx.x];
       int count = 0;
       for (int i = 0; i < len; ++i) count += (H[i] == t);
-      const float x = in[threadIdx.x];
+      const float x = __ldcg(in + threadIdx.x);
       out[threadIdx.x] = count ? penalize_value(x, count, pol) : x;
     }
   }
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(THREADS)
 
 // Copy the given candidate logits into the workspace copy unchanged (the
 // penalty kernel only rewrites them when penalties are active).
-__global__ void copy_q_kernel(ReqTable tab, int rows_total) {
+__global__ void copy_q_kernel(const __grid_constant__ ReqTable tab, int rows_total) {
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.x;

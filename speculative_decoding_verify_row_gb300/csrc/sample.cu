@@ -303,7 +303,7 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
 // The float whose order key is k (the inverse of float_key); NaN, whose key
 // is 0 whatever its bits, is read back from the row.
 __device__ __forceinline__ float value_of_key(uint32_t k, const float* row, int32_t id) {
-  if (k == 0u) return row[id];
+  if (k == 0u) return __ldcg(row + id);
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
@@ -410,7 +410,7 @@ __device__ bool segment_top64_fast(const float* __restrict__ rp, long long s0, l
 #pragma unroll
   for (int i = 0; i < PT; ++i) {
     const int e = i * THREADS + tid;
-    v[i] = ld_once(rp + s0 + (e < n_seg ? e : 0));
+    v[i] = ld_logit(rp + s0 + (e < n_seg ? e : 0));
   }
   uint32_t key[PT];
 #pragma unroll
@@ -448,7 +448,7 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = base + u * THREADS + tid;
-      t[u] = lists[i < total ? i : 0];               // unconditional: loads overlap
+      t[u] = __ldcg(lists + (i < total ? i : 0));    // unconditional: loads overlap
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -498,14 +498,50 @@ __device__ __forceinline__ int last_positive(const float* w, int m) {
 //      p(x) > 0).
 // Warp 0 applies the policy to the pool while warp 1 builds q, warp 2 draws
 // the row's two uniforms and warp 3 reads the draft token.
-__device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4* dec) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const vr_policy& pol = rq.pol;
-  const int local = row - rq.row0;
-  if (pol.temperature == 0.f) {
-    if (tid == 0) dec[row] = make_int4(rs.ids[0], rs.ids[0], rs.ids[0], 0);
+// q of a draft row, by warp 1: the node's candidates in pool order under the
+// request's policy, or the point mass on the draft when no candidates were
+// given (a candidate proposed without probabilities, e.g. by an n-gram match)
+__device__ __forceinline__ void build_q(const ReqDev& rq, int local, RowShared& rs) {
+  const int lane = threadIdx.x & 31;
+  if (!rq.q_ids) {
+    if (lane == 0) {
+      rs.qid[0] = rq.tokens[local];
+      rs.qp[0] = 1.0f;
+      rs.qm = 1;
+    }
     return;
   }
+  const float* qv = rq.q_pen + static_cast<size_t>(local) * kQCand;
+  const int32_t* qi = rq.q_ids + static_cast<size_t>(local) * kQCand;
+  // one load per lane, then ranks by shuffles (no loads inside the loop)
+  const int sl = lane < kQCand ? lane : 0;
+  const float v = __ldcg(qv + sl);         // possibly written by the penalty kernel
+  const int32_t id = qi[sl];
+  const uint32_t k = float_key(v);
+  int rank = 0;
+#pragma unroll
+  for (int s2 = 0; s2 < kQCand; ++s2) {
+    const uint32_t ks = __shfl_sync(0xffffffffu, k, s2);
+    const int32_t is = __shfl_sync(0xffffffffu, id, s2);
+    rank += ((ks > k) | ((ks == k) & ((is < id) | ((is == id) & (s2 < lane))))) ? 1 : 0;
+  }
+  if (lane < kQCand) {
+    rs.qid[rank] = id;
+    rs.qv[rank] = v;
+  }
+  __syncwarp();
+  policy_warp(rs.qv, kQCand, rq.pol, rs.qe, rs.qpc, &rs.qm, &rs.qS);
+  if (lane < rs.qm) rs.qp[lane] = __fdiv_rn(rs.qe[lane], rs.qS);
+}
+
+// The parts of a row's decision that need none of the row's logits: the
+// chain flag, the draft token, both uniforms and, if with_q, q.  The inputs
+// read here were all written before the window's first kernel ran, so the
+// row kernel does this before waiting for its predecessor.
+__device__ void prepare_row(const ReqDev& rq, int row, bool with_q, RowShared& rs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (rq.pol.temperature == 0.f) return;
+  const int local = row - rq.row0;
   if (tid == 0) rs.chain = 1;
   __syncthreads();
   if (rq.parent)
@@ -513,43 +549,37 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
       if (rq.parent[j] != j - 1) rs.chain = 0;
   __syncthreads();
   // sampled chains take the rejection test: against the draft candidates' q
-  // when given, else against q = delta(draft) (a candidate proposed without
-  // probabilities, e.g. by an n-gram match)
+  // when given, else against q = delta(draft)
   const bool reject_row = rs.chain && local < rq.n_nodes;
   const uint64_t urow = static_cast<uint64_t>(local);
-
-  if (warp == 0) {
-    policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
-  } else if (warp == 1 && reject_row && !rq.q_ids) {
-    if (lane == 0) {
-      rs.qid[0] = rq.tokens[local];
-      rs.qp[0] = 1.0f;
-      rs.qm = 1;
-    }
-  } else if (warp == 1 && reject_row) {
-    // q: the node's candidates in pool order, then the same policy
-    const float* qv = rq.q_pen + static_cast<size_t>(local) * kQCand;
-    const int32_t* qi = rq.q_ids + static_cast<size_t>(local) * kQCand;
-    if (lane < kQCand) {
-      const uint32_t k = float_key(qv[lane]);
-      const int32_t id = qi[lane];
-      int rank = 0;
-      for (int s2 = 0; s2 < kQCand; ++s2) {
-        const uint32_t ks = float_key(qv[s2]);
-        const int32_t is = qi[s2];
-        rank += (ks > k) || (ks == k && (is < id || (is == id && s2 < lane)));
-      }
-      rs.qid[rank] = id;
-      rs.qv[rank] = qv[lane];
-    }
-    __syncwarp();
-    policy_warp(rs.qv, kQCand, pol, rs.qe, rs.qpc, &rs.qm, &rs.qS);
-    if (lane < rs.qm) rs.qp[lane] = __fdiv_rn(rs.qe[lane], rs.qS);
+  if (warp == 1 && reject_row && with_q) {
+    build_q(rq, local, rs);
   } else if (warp == 2) {
     if (lane == 0) rs.u2 = uniform01(rq.seed, rq.position, urow, kPurposeEmit);
     if (lane == 1 && reject_row) rs.u1 = uniform01(rq.seed, rq.position, urow, kPurposeAccept);
   } else if (warp == 3 && lane == 0 && reject_row) {
     rs.draft = rq.tokens[local];
+  }
+  __syncthreads();
+}
+
+// The row's decisions (emit draw y, residual draw z, accept bit) once its
+// pool is known; prepare_row ran before, with q built there unless q_now.
+__device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShared& rs,
+                           int4* dec) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const vr_policy& pol = rq.pol;
+  const int local = row - rq.row0;
+  if (pol.temperature == 0.f) {
+    if (tid == 0) dec[row] = make_int4(rs.ids[0], rs.ids[0], rs.ids[0], 0);
+    return;
+  }
+  const bool reject_row = rs.chain && local < rq.n_nodes;
+
+  if (warp == 0) {
+    policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
+  } else if (warp == 1 && reject_row && q_now) {
+    build_q(rq, local, rs);
   }
   __syncthreads();
   if (warp != 0) return;
@@ -567,19 +597,27 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
     const int32_t xd = rs.draft;
     const int qm = rs.qm;
     // residual (p - q)+ over the kept entries; p(x) from the matching entry
+    // entries lane and lane + 32 side by side (both divisions in flight)
     float px = 0.0f;
-    for (int jj = lane; jj < kPool; jj += 32) {
-      float rj = 0.0f;
-      if (jj < m) {
-        const float pj = __fdiv_rn(rs.e[jj], S);
-        float qj = 0.0f;
-        for (int s2 = 0; s2 < qm; ++s2)
-          if (rs.qid[s2] == rs.ids[jj]) qj = __fadd_rn(qj, rs.qp[s2]);
-        const float d = __fsub_rn(pj, qj);
-        rj = d > 0.0f ? d : 0.0f;
-        if (rs.ids[jj] == xd) px = pj;
-      }
-      rs.r[jj] = rj;
+    int32_t qid[kQCand];
+    float qp[kQCand];
+#pragma unroll
+    for (int s2 = 0; s2 < kQCand; ++s2) {
+      qid[s2] = s2 < qm ? rs.qid[s2] : -1;
+      qp[s2] = s2 < qm ? rs.qp[s2] : 0.0f;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int jj = lane + 32 * h;
+      const int32_t id = rs.ids[jj];
+      const float pj = __fdiv_rn(rs.e[jj], S);
+      float qj = 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < kQCand; ++s2)
+        if (qid[s2] == id) qj = __fadd_rn(qj, qp[s2]);
+      const float d = __fsub_rn(pj, qj);
+      rs.r[jj] = (jj < m && d > 0.0f) ? d : 0.0f;
+      if (jj < m && id == xd) px = pj;
     }
     // pool ids are distinct: at most one lane holds p(x)
     for (int o = 16; o >= 1; o >>= 1) {
@@ -610,16 +648,18 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4
 // ---------------------------------------------------------------------------
 // acceptance walk of one request (thread 0 writes; the CTA validates)
 
-__device__ void accept_request(const ReqDev& rq, int vocab, const int4* dec, int32_t* status,
-                               AcceptShared& as) {
-  const int n = rq.n_nodes, R = n + 1, tid = threadIdx.x;
+// The request's tokens and parents into shared memory, checked: bad token,
+// bad parent or bad candidate id bits in as.bad, as.not_chain if any node
+// does not hang from its predecessor.  Reads inputs only, so the row kernel
+// does it before waiting for its predecessor.
+__device__ void prepare_accept(const ReqDev& rq, int vocab, AcceptShared& as) {
+  const int n = rq.n_nodes, tid = threadIdx.x;
   const bool greedy = rq.pol.temperature == 0.f;
   if (tid == 0) {
     as.bad = 0;
     as.not_chain = 0;
   }
   __syncthreads();
-  for (int j = tid; j < R; j += THREADS) as.d[j] = dec[rq.row0 + j];
   if (tid < n) {
     const int t = rq.tokens[tid];
     const int p = rq.parent ? rq.parent[tid] : tid - 1;
@@ -638,6 +678,17 @@ __device__ void accept_request(const ReqDev& rq, int vocab, const int4* dec, int
       const int id = rq.q_ids[i];
       if (id < 0 || id >= vocab) atomicOr(&as.bad, VR_DEV_BAD_QID);
     }
+  __syncthreads();
+}
+
+// The acceptance walk of one request (thread 0 writes), after
+// prepare_accept, with every row's decisions in dec.
+__device__ void accept_request(const ReqDev& rq, const int4* dec, int32_t* status,
+                               AcceptShared& as) {
+  const int n = rq.n_nodes, R = n + 1, tid = threadIdx.x;
+  const bool greedy = rq.pol.temperature == 0.f;
+  const bool rejection = !greedy && !as.not_chain;
+  for (int j = tid; j < R; j += THREADS) as.d[j] = __ldcg(dec + rq.row0 + j);
   __syncthreads();
   if (tid != 0) return;
   if (as.bad) {
@@ -707,6 +758,7 @@ struct SampleArgs {
   int4* dec;               // [rows]
   int32_t* status;
   int decide;              // 0: pools only
+  int q_after_wait;        // q logits written by a predecessor (penalised q)
 };
 
 // sh.out[0..count) -> sh.sorted in pool order (zero-padded)
@@ -729,7 +781,7 @@ __device__ __forceinline__ void sort_out_into_sorted(SelectShared& sh) {
 // values, then the row's decisions, then (last row of its request) the
 // acceptance walk.
 __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, const uint64_t* pool,
-                           RowShared& rs, AcceptShared& as, int& last) {
+                           RowShared& rs, AcceptShared& as, int& last, bool prepared) {
   const int tid = threadIdx.x;
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const int n = a.vocab < kPool ? a.vocab : kPool;
@@ -751,7 +803,8 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
   __syncthreads();
   const int b = request_of_row(tab, row);
   const ReqDev& rq = request(tab, b);
-  decide_row(rq, row, n, rs, a.dec);
+  if (!prepared) prepare_row(rq, row, true, rs);
+  decide_row(rq, row, n, prepared && a.q_after_wait, rs, a.dec);
 
   // the last row of the request to finish walks the request
   __threadfence();
@@ -762,7 +815,8 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
   if (!last) return;
   __threadfence();
   if (tid == 0) a.req_ticket[b] = 0u;
-  accept_request(rq, a.vocab, a.dec, a.status, as);
+  if (!prepared) prepare_accept(rq, a.vocab, as);
+  accept_request(rq, a.dec, a.status, as);
 }
 
 // ---------------------------------------------------------------------------
@@ -770,7 +824,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
 
 
 __global__ void __launch_bounds__(THREADS, 2)
-    sample_kernel(SampleArgs a, ReqTable tab) {
+    sample_kernel(const __grid_constant__ SampleArgs a, const __grid_constant__ ReqTable tab) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   StageShared& st = *reinterpret_cast<StageShared*>(dyn_smem);
   __shared__ RowShared rs;
@@ -800,7 +854,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int i = 0; i < SUB / THREADS; ++i) {
         const long long e = b + i * THREADS + tid;
-        f[i] = __ldg(rp + (e < s1 ? e : b));          // unconditional: loads overlap
+        f[i] = __ldcg(rp + (e < s1 ? e : b));         // unconditional: loads overlap
       }
 #pragma unroll
       for (int i = 0; i < SUB / THREADS; ++i) {
@@ -828,7 +882,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (tid == 0) a.row_ticket[row] = 0u;
   const uint64_t* pool =
       merge_lists(a.cand + static_cast<size_t>(row) * a.nseg * kPool, a.nseg, st.mrg);
-  finish_row(a, tab, row, pool, rs, as, last);
+  finish_row(a, tab, row, pool, rs, as, last, false);
 }
 
 // Sampling stage for rows whose group maxima (largest order key per 32
@@ -840,7 +894,8 @@ __global__ void __launch_bounds__(THREADS, 2)
 //      gathered and their top 64 taken;
 //  (c) pool, policy, decisions and acceptance as in sample_kernel.
 __global__ void __launch_bounds__(THREADS, 1)
-    sample_rows_kernel(SampleArgs a, ReqTable tab, const uint32_t* __restrict__ gmax,
+    sample_rows_kernel(const __grid_constant__ SampleArgs a, const __grid_constant__ ReqTable tab,
+                       const uint32_t* __restrict__ gmax,
                        int ngroups) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   RowsShared& sr = *reinterpret_cast<RowsShared*>(dyn_smem);
@@ -849,8 +904,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ AcceptShared as;
   __shared__ int last;
   pdl_trigger();
-  pdl_wait();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // before the wait: everything of the row's decision that needs no logits
+  // (this kernel only runs after the window's first kernel, which triggers
+  // its dependents only once its own predecessors are complete)
+  {
+    const ReqDev& rq = request(tab, request_of_row(tab, row));
+    prepare_row(rq, row, !a.q_after_wait, rs);
+    prepare_accept(rq, a.vocab, as);
+  }
+  pdl_wait();
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
 
@@ -861,7 +924,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int i = 0; i < GI_MAX; ++i) {
       const int g = i * THREADS + tid;
-      gk[i] = __ldg(gm + (g < ngroups ? g : 0));      // unconditional: loads overlap
+      gk[i] = __ldcg(gm + (g < ngroups ? g : 0));     // unconditional: loads overlap
     }
     if (!keys_top64(gk, ngroups - tid, static_cast<uint32_t>(tid), sr.fast)) {
       uint64_t x[GI_MAX];
@@ -888,7 +951,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   for (int t = 0; t < GPW; ++t) {
     const int j = warp + t * (THREADS / 32);
     const long long v = static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
-    fv[t] = __ldg(rp + (v < a.vocab ? v : 0));        // unconditional: loads overlap
+    fv[t] = __ldcg(rp + (v < a.vocab ? v : 0));       // unconditional: loads overlap
   }
   uint32_t kv[GPW];
 #pragma unroll
@@ -930,7 +993,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (tid < kPool) pool[tid] = sh.sorted[tid];
     __syncthreads();
   }
-  finish_row(a, tab, row, pool, rs, as, last);
+  finish_row(a, tab, row, pool, rs, as, last, true);
 }
 
 __global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len, vr_policy pol,
@@ -998,6 +1061,7 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.dec = dec;
   a.status = status;
   a.decide = tab ? 1 : 0;
+  a.q_after_wait = 1;
   const size_t smem = sizeof(smp::StageShared);
   static bool attr_set = false;
   if (!attr_set) {
@@ -1019,7 +1083,8 @@ bool sample_rows_supported(int vocab) {
 
 int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t* gmax,
                        uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
-                       const ReqTable& tab, int4* dec, int32_t* status, cudaStream_t stream) {
+                       const ReqTable& tab, int4* dec, int32_t* status, bool q_after_wait,
+                       cudaStream_t stream) {
   smp::SampleArgs a{};
   a.logits = logits;
   a.vocab = vocab;
@@ -1030,6 +1095,7 @@ int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t*
   a.dec = dec;
   a.status = status;
   a.decide = 1;
+  a.q_after_wait = q_after_wait ? 1 : 0;
   const size_t smem = sizeof(smp::RowsShared);
   static bool attr_set = false;
   if (!attr_set) {

@@ -71,20 +71,15 @@ __device__ __forceinline__ bool penalties_active(const vr_policy& p) {
 // total order of float32 used by the pool: unsigned order of the key below
 // is value order with every NaN lowest and -0.0 below +0.0.
 
-// A float read the compiler must keep: the asm is volatile, so the load is
-// issued once where written and its value held in a register, never dropped
-// and re-read later under register pressure (which a plain read-only load
-// may be).  Read-only path, no L1 allocation: the data is read once.
-__device__ __forceinline__ float ld_once(const float* p) {
+// Loads of data a preceding kernel of the same window wrote (logits, group
+// maxima).  With programmatic dependent launch a kernel can be resident
+// before its predecessor finishes, so these go through L2 only (.cg), never
+// through a possibly stale L1 line.  ld_logit is volatile: issued where
+// written and its value held in a register, never dropped and re-read later
+// under register pressure.
+__device__ __forceinline__ float ld_logit(const float* p) {
   float v;
-  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
-// The same for data read again soon (allocated in L1).
-__device__ __forceinline__ float ld_once_l1(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 
@@ -204,30 +199,47 @@ __device__ __forceinline__ int warp_first(int m, Pred pred) {
   return b ? 32 + __ffs(b) - 1 : -1;
 }
 
-// running sums c[j] = w_0 + ... + w_j for j < n, sequential, by one lane;
-// w and c 16-byte aligned
-__device__ __forceinline__ void running_sums(const float* w, float* c, int n) {
-  float acc = 0.0f;
-  int j = 0;
-  for (; j + 4 <= n; j += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(w + j);
-    acc = __fadd_rn(acc, v.x);
-    c[j] = acc;
-    acc = __fadd_rn(acc, v.y);
-    c[j + 1] = acc;
-    acc = __fadd_rn(acc, v.z);
-    c[j + 2] = acc;
-    acc = __fadd_rn(acc, v.w);
-    c[j + 3] = acc;
+// running sums c[j] = w_0 + ... + w_j for j < n <= N, sequential, by one
+// lane; w and c are 16-byte aligned arrays of at least N floats.  All N
+// weights are read first (no load waits inside the chain of additions);
+// entries past n count as zero, so c[j] for j >= n repeats c[n - 1].
+template <int N>
+__device__ __forceinline__ void running_sums_n(const float* w, float* c, int n) {
+  float v[N];
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(w + j);
+    v[j] = t.x;
+    v[j + 1] = t.y;
+    v[j + 2] = t.z;
+    v[j + 3] = t.w;
   }
-  for (; j < n; ++j) {
-    acc = __fadd_rn(acc, w[j]);
-    c[j] = acc;
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    float4 o;
+    acc = __fadd_rn(acc, j < n ? v[j] : 0.0f);
+    o.x = acc;
+    acc = __fadd_rn(acc, j + 1 < n ? v[j + 1] : 0.0f);
+    o.y = acc;
+    acc = __fadd_rn(acc, j + 2 < n ? v[j + 2] : 0.0f);
+    o.z = acc;
+    acc = __fadd_rn(acc, j + 3 < n ? v[j + 3] : 0.0f);
+    o.w = acc;
+    *reinterpret_cast<float4*>(c + j) = o;
   }
 }
 
+__device__ __forceinline__ void running_sums(const float* w, float* c, int n) {
+  if (n <= 8)
+    running_sums_n<8>(w, c, n);
+  else
+    running_sums_n<64>(w, c, n);
+}
+
 // e and pc must be 16-byte aligned shared arrays of kPool floats
-__device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_policy& pol,
+// pol by value: its fields live in registers for the whole function
+__device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_policy pol,
                                             float* e, float* pc, int* m_out, float* S_out) {
   const int lane = threadIdx.x & 31;
   int K = topk_limit(pol.top_k);
@@ -247,19 +259,18 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
   }
   const float T = pol.temperature;
   const float v0 = vals[0];
-  for (int j = lane; j < kPool; j += 32) {
-    float ej = 0.0f;
-    if (j == 0) {
-      ej = 1.0f;
-    } else if (j < K) {
-      const float v = vals[j];
-      if (!(isnan(v) || v == -__int_as_float(0x7f800000))) {
-        const float z = __fdiv_rn(__fsub_rn(v, v0), T);
-        ej = (z >= -87.0f) ? vexp(z) : 0.0f;
-      }
-    }
-    e[j] = ej;
-  }
+  // entry lane, and entry lane + 32 only when the kept count reaches past
+  // 32 (a warp-uniform test); no branches inside an entry
+  auto weight = [&](int j) {
+    const float v = vals[j];
+    const float z = __fdiv_rn(__fsub_rn(v, v0), T);
+    const bool live = (j >= 1) & (j < K) & !isnan(v) & (v != -__int_as_float(0x7f800000)) &
+                      (z >= -87.0f);
+    const float ex = vexp(z);
+    return j == 0 ? 1.0f : (live ? ex : 0.0f);
+  };
+  e[lane] = weight(lane);
+  e[lane + 32] = K > 32 ? weight(lane + 32) : 0.0f;
   __syncwarp();
   if (lane == 0) running_sums(e, pc, K);
   __syncwarp();
@@ -285,12 +296,17 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
 }
 
 // ---------------------------------------------------------------------------
-// programmatic dependent launch.  Every kernel of the library lets the next
-// kernel on the stream start launching at once (launch_dependents) and waits
-// for its predecessor grid to complete before it touches any buffer that a
-// predecessor may write or read (wait).  Since each kernel waits for the
-// previous one, completion still follows stream order; only launch latency
-// and prologues overlap.  Without the launch attribute both are no-ops.
+// programmatic dependent launch.  Every kernel of the library waits for its
+// predecessor grid to complete (wait) before it touches any buffer that a
+// predecessor may write or read, and lets the next kernel on the stream
+// start launching early (launch_dependents): at once, except the kernels
+// that start a window (the projections and their split passes), which
+// trigger only after their own wait.  So every later kernel of a window
+// starts after everything before the window is complete and may read the
+// window's inputs (drafts, candidates, parents) before its own wait, as the
+// row sampling kernel does.  Completion still follows stream order; only
+// launch latency and prologues overlap.  Without the launch attribute both
+// are no-ops.
 
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
