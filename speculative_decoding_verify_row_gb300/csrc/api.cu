@@ -135,16 +135,26 @@ ReqTable single(const ReqDev& r) {
 
 
 // gmax (nullable): where the tensor-core paths also record the group maxima
+// logits2 (nullable): a second buffer receiving the same logits (the
+// tensor-core epilogues write both; the CUDA-core path copies)
 int project(const uint16_t* weight, const float* act, int rows, int hidden, int vocab, int path,
-            float* logits, uint32_t* gmax, void* ws, const Layout& L, cudaStream_t s) {
+            float* logits, float* logits2, uint32_t* gmax, void* ws, const Layout& L,
+            cudaStream_t s) {
   if (path == VR_PATH_AUTO) path = VR_PATH_TC;
   if (path == VR_PATH_TC)
-    return launch_project_tc(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
-                             gmax, at<int32_t>(ws, L.status), s);
+    return launch_project_tc(weight, act, rows, hidden, vocab, logits, logits2,
+                             at<void>(ws, L.planes), gmax, at<int32_t>(ws, L.status), s);
   if (path == VR_PATH_TC_BATCH)
-    return launch_project_tcb(weight, act, rows, hidden, vocab, logits, at<void>(ws, L.planes),
-                              gmax, at<int32_t>(ws, L.status), s);
-  if (path == VR_PATH_FFMA) return launch_project_ffma(weight, act, rows, hidden, vocab, logits, s);
+    return launch_project_tcb(weight, act, rows, hidden, vocab, logits, logits2,
+                              at<void>(ws, L.planes), gmax, at<int32_t>(ws, L.status), s);
+  if (path == VR_PATH_FFMA) {
+    const int st = launch_project_ffma(weight, act, rows, hidden, vocab, logits, s);
+    if (st != VR_OK || !logits2) return st;
+    return cudaMemcpyAsync(logits2, logits, static_cast<size_t>(rows) * vocab * sizeof(float),
+                           cudaMemcpyDeviceToDevice, s) == cudaSuccess
+               ? VR_OK
+               : VR_ERR_CUDA;
+  }
   return VR_ERR_ARG;
 }
 
@@ -184,16 +194,12 @@ int window_device(const uint16_t* weight, const float* act, int rows, int hidden
                   float* pen_logits, int32_t* out_ids, int32_t* out_accept, int32_t* out_n,
                   void* ws, const Layout& L, cudaStream_t s) {
   uint32_t* gmax = records_gmax(path, vocab) ? at<uint32_t>(ws, L.gmax) : nullptr;
-  int st = project(weight, act, rows, hidden, vocab, path, logits, gmax, ws, L, s);
-  if (st != VR_OK) return st;
   const bool act_pen = active(pol);
-  float* target = logits;
-  if (act_pen && pen_logits) {
-    if (cudaMemcpyAsync(pen_logits, logits, static_cast<size_t>(rows) * vocab * sizeof(float),
-                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-      return VR_ERR_CUDA;
-    target = pen_logits;
-  }
+  // penalties into a separate buffer: the projection writes both copies
+  float* target = (act_pen && pen_logits) ? pen_logits : logits;
+  int st = project(weight, act, rows, hidden, vocab, path, logits,
+                   target != logits ? target : nullptr, gmax, ws, L, s);
+  if (st != VR_OK) return st;
   float* q_pen = (act_pen && q_ids) ? at<float>(ws, L.q_pen) : const_cast<float*>(q_logits);
   const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_pen, hist,
                                        hist_len, pol, seed, position, out_ids, out_accept, out_n));
@@ -245,7 +251,7 @@ int vr_verify_project(const uint16_t* weight, const float* act, int rows, int hi
   if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH) return VR_ERR_ARG;
   if (!aligned16(weight)) return VR_ERR_ARG;
   if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
-  return project(weight, act, rows, hidden, vocab, path, logits, nullptr, ws,
+  return project(weight, act, rows, hidden, vocab, path, logits, nullptr, nullptr, ws,
                  layout(rows, hidden, vocab), static_cast<cudaStream_t>(stream));
 }
 
@@ -384,15 +390,11 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
     return VR_ERR_CUDA;
 
   uint32_t* gmax = records_gmax(path, vocab) ? at<uint32_t>(ws, L.gmax) : nullptr;
-  st = project(weight, act, rows, hidden, vocab, path, logits, gmax, ws, L, s);
+  // penalties into a separate buffer: the projection writes both copies
+  float* target = (any_active && pen_logits) ? pen_logits : logits;
+  st = project(weight, act, rows, hidden, vocab, path, logits, target != logits ? target : nullptr,
+               gmax, ws, L, s);
   if (st != VR_OK) return st;
-  float* target = logits;
-  if (any_active && pen_logits) {
-    if (cudaMemcpyAsync(pen_logits, logits, static_cast<size_t>(rows) * vocab * sizeof(float),
-                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-      return VR_ERR_CUDA;
-    target = pen_logits;
-  }
   ReqTable tab{};
   tab.many = at<ReqDev>(ws, L.reqs);
   tab.row_req = at<int32_t>(ws, L.row_req);

@@ -129,27 +129,13 @@ __global__ void __launch_bounds__(THREADS)
   }
 }
 
-// Copy the given candidate logits into the workspace copy unchanged (the
-// penalty kernel only rewrites them when penalties are active).
-__global__ void copy_q_kernel(const __grid_constant__ ReqTable tab, int rows_total) {
-  pdl_trigger();
-  pdl_wait();
-  const int g = blockIdx.x;
-  const ReqDev& rq = request(tab, request_of_row(tab, g));
-  const int local = g - rq.row0;
-  if (!rq.q_ids || local >= rq.n_nodes || rq.q_pen == rq.q_logits_in) return;
-  if (threadIdx.x < kQCand)
-    rq.q_pen[static_cast<size_t>(local) * kQCand + threadIdx.x] =
-        rq.q_logits_in[static_cast<size_t>(local) * kQCand + threadIdx.x];
-}
-
 }  // namespace pen
 
+// A request's q copy in the workspace exists only when its penalties are
+// active, and then the q blocks write all 8 candidates (penalised or not),
+// so no separate copy pass is needed.
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab, bool with_q,
                     uint32_t* gmax, int32_t* status, cudaStream_t stream) {
-  if (with_q && launch_pdl(pen::copy_q_kernel, dim3(rows_total), dim3(32), 0, stream, tab,
-                          rows_total) != cudaSuccess)
-    return VR_ERR_CUDA;
   const int blocks = rows_total * (with_q ? 2 : 1);
   return launch_pdl(pen::penalize_kernel, dim3(blocks), dim3(pen::THREADS), 0, stream, tab,
                     rows_total, logits, vocab, with_q ? 1 : 0, gmax, status) == cudaSuccess

@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_x, int hidden, int vocab,
                       int rows_in_group, int row_base, float* __restrict__ logits,
-                      uint32_t* __restrict__ gmax, int ngroups, int32_t* status) {
+                      float* __restrict__ logits2, uint32_t* __restrict__ gmax, int ngroups,
+                      int32_t* status) {
   constexpr bool kFused = NIT > 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -409,7 +410,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int r = rb + i;
             if (r < rows_in_group) {
               const float x = __fadd_rn(__fadd_rn(hi[i], mid[i]), lo[i]);
-              if (v < vocab) logits[static_cast<size_t>(row_base + r) * vocab + v] = x;
+              if (v < vocab) {
+                const size_t at = static_cast<size_t>(row_base + r) * vocab + v;
+                logits[at] = x;
+                if (logits2) logits2[at] = x;     // a second copy (penalised in place later)
+              }
               if (gmax && vbase < vocab) {
                 // the largest order key of these 32 vocabulary rows
                 const uint32_t k =
@@ -495,8 +500,8 @@ namespace {
 
 template <int NIT>
 cudaError_t launch_group(const CUtensorMap& tm_w, const CUtensorMap& tm_x, int hidden, int vocab,
-                         int rg, int row_base, float* logits, uint32_t* gmax, int32_t* status,
-                         int grid, cudaStream_t stream) {
+                         int rg, int row_base, float* logits, float* logits2, uint32_t* gmax,
+                         int32_t* status, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -505,7 +510,7 @@ cudaError_t launch_group(const CUtensorMap& tm_w, const CUtensorMap& tm_x, int h
     attr_set = true;
   }
   return launch_pdl(tc::project_tc_kernel<NIT>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES,
-                    stream, tm_w, tm_x, hidden, vocab, rg, row_base, logits, gmax,
+                    stream, tm_w, tm_x, hidden, vocab, rg, row_base, logits, logits2, gmax,
                     (vocab + 31) / 32, status);
 }
 
@@ -519,8 +524,8 @@ size_t tc_scratch_bytes(int rows, int hidden) {
 }
 
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                      float* logits, void* scratch, uint32_t* gmax, int32_t* status,
-                      cudaStream_t stream) {
+                      float* logits, float* logits2, void* scratch, uint32_t* gmax,
+                      int32_t* status, cudaStream_t stream) {
   if (!g_num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return VR_ERR_CUDA;
@@ -548,11 +553,14 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
     const int nit = (rows * (tc::BK / 8) + 31) / 32;
     cudaError_t e;
     if (nit <= 1)
-      e = launch_group<1>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+      e = launch_group<1>(tm_w, tm_a, hidden, vocab, rows, 0, logits, logits2, gmax, status, grid,
+                          stream);
     else if (nit <= 2)
-      e = launch_group<2>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+      e = launch_group<2>(tm_w, tm_a, hidden, vocab, rows, 0, logits, logits2, gmax, status, grid,
+                          stream);
     else
-      e = launch_group<4>(tm_w, tm_a, hidden, vocab, rows, 0, logits, gmax, status, grid, stream);
+      e = launch_group<4>(tm_w, tm_a, hidden, vocab, rows, 0, logits, logits2, gmax, status, grid,
+                          stream);
     if (e != cudaSuccess) return VR_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;
   }
@@ -575,8 +583,8 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
                           tc::BK, tc::BN))
       return VR_ERR_ARG;
     const int rg = std::min(tc::NP, rows - g * tc::NP);
-    if (launch_group<0>(tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, gmax, status, grid,
-                        stream) != cudaSuccess)
+    if (launch_group<0>(tm_w, tm_b, hidden, vocab, rg, g * tc::NP, logits, logits2, gmax, status,
+                        grid, stream) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VR_OK : VR_ERR_CUDA;

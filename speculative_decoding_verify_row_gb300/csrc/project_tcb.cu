@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     project_tcb_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_a, int hidden, int vocab,
                        int rows_in_group, int row_base, float* __restrict__ logits,
-                       int vec_ok, uint32_t* __restrict__ gmax, int ngroups, int32_t* status) {
+                       float* __restrict__ logits2, int vec_ok, uint32_t* __restrict__ gmax,
+                       int ngroups, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -208,6 +209,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int mh = 0; mh < MH; ++mh) {
         const int rl = mh * BM + quarter * 32 + lane;           // row within the group
         float* out = logits + static_cast<size_t>(row_base + rl) * vocab;
+        // a second copy of the row (penalised in place later), or none
+        float* out2 = logits2 ? logits2 + static_cast<size_t>(row_base + rl) * vocab : nullptr;
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(tmem_base + lane_off + mh * BN + c * 32, v);
@@ -229,9 +232,17 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int i = 0; i < 8; ++i)
                 *reinterpret_cast<float4*>(out + v0 + 4 * i) =
                     make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              if (out2)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  *reinterpret_cast<float4*>(out2 + v0 + 4 * i) =
+                      make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             } else {
               for (int i = 0; i < 32; ++i)
                 if (v0 + i < vocab) out[v0 + i] = v[i];
+              if (out2)
+                for (int i = 0; i < 32; ++i)
+                  if (v0 + i < vocab) out2[v0 + i] = v[i];
             }
           }
         }
@@ -297,8 +308,8 @@ size_t tcb_plane_bytes(int rows, int hidden) {
 }
 
 int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                       float* logits, void* planes, uint32_t* gmax, int32_t* status,
-                       cudaStream_t stream) {
+                       float* logits, float* logits2, void* planes, uint32_t* gmax,
+                       int32_t* status, cudaStream_t stream) {
   if (!g_tcb_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -326,7 +337,8 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
   if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tcb::BK, tcb::BN)) return VR_ERR_ARG;
   const int n_tiles = (vocab + tcb::BN - 1) / tcb::BN;
   const int grid = std::min(n_tiles, g_tcb_sms);
-  const int vec_ok = (vocab % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+  const int vec_ok = (vocab % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(logits2) % 16 == 0);
   for (int g = 0; g < groups; ++g) {
     CUtensorMap tm_a;
     if (!encode_bf16_tile(&tm_a, pl + static_cast<size_t>(g) * tcb::NPLANE * tcb::GROUP * hidden,
@@ -334,8 +346,8 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
       return VR_ERR_ARG;
     const int rg = std::min(tcb::GROUP, rows - g * tcb::GROUP);
     if (launch_pdl(tcb::project_tcb_kernel, dim3(grid), dim3(tcb::THREADS), tcb::SMEM_BYTES,
-                   stream, tm_w, tm_a, hidden, vocab, rg, g * tcb::GROUP, logits, vec_ok,
-                   gmax, (vocab + 31) / 32, status) != cudaSuccess)
+                   stream, tm_w, tm_a, hidden, vocab, rg, g * tcb::GROUP, logits, logits2,
+                   vec_ok, gmax, (vocab + 31) / 32, status) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return VR_OK;

@@ -15,15 +15,16 @@ bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64
                       uint32_t box_inner, uint32_t box_outer);
 size_t tcb_plane_bytes(int rows, int hidden);
 // gmax (nullable): [rows][ceil(vocab/32)] largest order key per 32 vocab rows
+// logits2 (nullable): a second buffer receiving the same logits
 int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                       float* logits, void* planes, uint32_t* gmax, int32_t* status,
-                       cudaStream_t stream);
+                       float* logits, float* logits2, void* planes, uint32_t* gmax,
+                       int32_t* status, cudaStream_t stream);
 // scratch (tc_scratch_bytes, 16-byte aligned): the activation planes for
 // more than 16 rows, else room for an aligned copy of act
 size_t tc_scratch_bytes(int rows, int hidden);
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
-                      float* logits, void* scratch, uint32_t* gmax, int32_t* status,
-                      cudaStream_t stream);
+                      float* logits, float* logits2, void* scratch, uint32_t* gmax,
+                      int32_t* status, cudaStream_t stream);
 int ffma_rows_per_pass(int hidden);
 int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                         float* logits, cudaStream_t stream);
