@@ -169,17 +169,18 @@ bool records_gmax(int path, int vocab) {
 int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* target,
                   uint32_t* gmax, bool any_active, bool any_q, void* ws, const Layout& L,
                   cudaStream_t s) {
+  (void)n_req;
+  // windows on a tensor-core path: the row kernel applies the penalties itself
+  if (gmax)
+    return launch_sample_rows(target, rows, vocab, gmax, at<uint32_t>(ws, L.status + kReqTicketOff),
+                              at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
+                              at<int4>(ws, L.dec), at<int32_t>(ws, L.status),
+                              any_active && any_q, any_active ? target : nullptr, s);
   int st;
   if (any_active) {
     st = launch_penalize(tab, rows, target, vocab, any_q, gmax, at<int32_t>(ws, L.status), s);
     if (st != VR_OK) return st;
   }
-  (void)n_req;
-  if (gmax)
-    return launch_sample_rows(target, rows, vocab, gmax, at<uint32_t>(ws, L.status + kReqTicketOff),
-                              at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
-                              at<int4>(ws, L.dec), at<int32_t>(ws, L.status),
-                              any_active && any_q, s);
   return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
                        at<uint32_t>(ws, L.status + kReqTicketOff), at<int32_t>(ws, L.pool_ids),

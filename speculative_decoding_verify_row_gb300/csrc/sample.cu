@@ -88,6 +88,10 @@ struct RowsShared {
   uint64_t cands[C_MAX];
   uint64_t pool[kPool];
   int ccount;
+  // the row's penalty history (built before the wait)
+  int32_t H[VR_MAX_PENALTY_WINDOW];
+  int32_t path[VR_MAX_WINDOW_ROWS];
+  int h_len, h_bad;
 };
 
 struct RowShared {
@@ -515,7 +519,7 @@ __device__ __forceinline__ void build_q(const ReqDev& rq, int local, RowShared& 
   const int32_t* qi = rq.q_ids + static_cast<size_t>(local) * kQCand;
   // one load per lane, then ranks by shuffles (no loads inside the loop)
   const int sl = lane < kQCand ? lane : 0;
-  const float v = __ldcg(qv + sl);         // possibly written by the penalty kernel
+  const float v = __ldcg(qv + sl);         // possibly penalised earlier in this window
   const int32_t id = qi[sl];
   const uint32_t k = float_key(v);
   int rank = 0;
@@ -758,7 +762,8 @@ struct SampleArgs {
   int4* dec;               // [rows]
   int32_t* status;
   int decide;              // 0: pools only
-  int q_after_wait;        // q logits written by a predecessor (penalised q)
+  int q_after_wait;        // q logits penalised in this window (built after the wait)
+  float* pen_logits;       // row kernel: penalties applied in place here (== logits), or null
 };
 
 // sh.out[0..count) -> sh.sorted in pool order (zero-padded)
@@ -885,6 +890,99 @@ __global__ void __launch_bounds__(THREADS, 2)
   finish_row(a, tab, row, pool, rs, as, last, false);
 }
 
+// ---------------------------------------------------------------------------
+// penalties inside the row kernel ("Speculative decoding on RDNA" §04): the
+// same arithmetic as the penalty kernel, for the CTA's own row
+
+// H of target row `local`: the last W tokens of (hist || tokens on the path
+// root -> node local - 1).  Thread 0 walks the ancestors, all threads copy.
+// Sets sr.h_len, and sr.h_bad for a parent array that is not topological.
+__device__ void build_row_history(const ReqDev& rq, int local, RowsShared& sr) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    int n = 0, node = local - 1, steps = 0, bad = 0;
+    while (node >= 0) {
+      if (node >= rq.n_nodes || steps > rq.n_nodes) {
+        bad = 1;
+        break;
+      }
+      sr.path[n++] = rq.tokens[node];
+      const int p = rq.parent ? rq.parent[node] : node - 1;
+      if (p >= node || p < -1) {
+        bad = 1;
+        break;
+      }
+      node = p;
+      ++steps;
+    }
+    sr.h_bad = bad;
+    sr.h_len = n;          // path length for now
+  }
+  __syncthreads();
+  const int n = sr.h_len, W = rq.pol.window;
+  const int from_path = sr.h_bad ? 0 : min(n, W);
+  const int from_hist = sr.h_bad ? 0 : min(rq.hist_len, W - from_path);
+  for (int i = tid; i < from_hist; i += THREADS) sr.H[i] = rq.hist[rq.hist_len - from_hist + i];
+  for (int i = tid; i < from_path; i += THREADS) sr.H[from_hist + i] = sr.path[from_path - 1 - i];
+  __syncthreads();
+  if (tid == 0) sr.h_len = from_hist + from_path;
+  __syncthreads();
+}
+
+// Penalise the CTA's row in place (each distinct token of H once), refresh
+// the group maxima the penalties touched, and write the penalised copy of
+// the draft candidates of node `local` (a chain's node is checked against
+// this row).  Runs after the wait.
+__device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vocab,
+                                 uint32_t* gmax_row, RowsShared& sr) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const vr_policy& pol = rq.pol;
+  const int len = sr.h_len;
+  for (int j = tid; j < len; j += THREADS) {
+    const int t = sr.H[j];
+    bool first = true;
+    int count = 0;
+    for (int i = 0; i < len; ++i) {
+      if (sr.H[i] == t) {
+        ++count;
+        if (i < j) first = false;
+      }
+    }
+    if (first && t >= 0 && t < vocab) row[t] = penalize_value(__ldcg(row + t), count, pol);
+  }
+  __threadfence();     // the rewritten logits reach L2 before anyone reads them there
+  __syncthreads();
+  // a warp per history slot: the first slot of each touched group refreshes
+  // that group's maximum from the penalised row
+  for (int j = warp; j < len; j += THREADS / 32) {
+    const int t = sr.H[j];
+    if (t < 0 || t >= vocab) continue;
+    const int g = t >> 5;
+    bool seen = false;
+    for (int i = lane; i < j; i += 32) {
+      const int u = sr.H[i];
+      seen |= (u >= 0) & (u < vocab) & ((u >> 5) == g);
+    }
+    if (__any_sync(0xffffffffu, seen)) continue;
+    const int v = g * 32 + lane;
+    const uint32_t k = v < vocab ? float_key(__ldcg(row + v)) : 0u;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, k);
+    if (lane == 0) gmax_row[g] = m;
+  }
+  // the node's draft candidates, penalised with this row's history
+  const bool chain_node = rq.q_ids && local < rq.n_nodes &&
+                          (!rq.parent || rq.parent[local] == local - 1);
+  if (chain_node && tid < kQCand) {
+    const int32_t t = rq.q_ids[static_cast<size_t>(local) * kQCand + tid];
+    int count = 0;
+    for (int i = 0; i < len; ++i) count += (sr.H[i] == t);
+    const float x = __ldcg(rq.q_logits_in + static_cast<size_t>(local) * kQCand + tid);
+    rq.q_pen[static_cast<size_t>(local) * kQCand + tid] = count ? penalize_value(x, count, pol) : x;
+  }
+  __threadfence();     // group maxima and q reach L2 before they are read there
+  __syncthreads();
+}
+
 // Sampling stage for rows whose group maxima (largest order key per 32
 // vocabulary rows) were recorded by the projection: one CTA per row.
 //  (a) the row's 64 groups with the largest maxima (ties: lower group index),
@@ -895,8 +993,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 //  (c) pool, policy, decisions and acceptance as in sample_kernel.
 __global__ void __launch_bounds__(THREADS, 1)
     sample_rows_kernel(const __grid_constant__ SampleArgs a, const __grid_constant__ ReqTable tab,
-                       const uint32_t* __restrict__ gmax,
-                       int ngroups) {
+                       uint32_t* __restrict__ gmax, int ngroups) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   RowsShared& sr = *reinterpret_cast<RowsShared*>(dyn_smem);
   SelectShared& sh = sr.sel;
@@ -908,14 +1005,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   // before the wait: everything of the row's decision that needs no logits
   // (this kernel only runs after the window's first kernel, which triggers
   // its dependents only once its own predecessors are complete)
-  {
-    const ReqDev& rq = request(tab, request_of_row(tab, row));
-    prepare_row(rq, row, !a.q_after_wait, rs);
-    prepare_accept(rq, a.vocab, as);
-  }
+  const ReqDev& rq0 = request(tab, request_of_row(tab, row));
+  const bool pen = a.pen_logits && penalties_active(rq0.pol);
+  prepare_row(rq0, row, !a.q_after_wait, rs);
+  prepare_accept(rq0, a.vocab, as);
+  if (pen) build_row_history(rq0, row - rq0.row0, sr);
   pdl_wait();
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
+  if (pen) {
+    if (sr.h_bad && tid == 0) set_status(a.status, VR_DEV_BAD_PARENT);
+    penalize_own_row(rq0, row - rq0.row0, a.pen_logits + static_cast<size_t>(row) * a.vocab,
+                     a.vocab, gmax + static_cast<size_t>(row) * ngroups, sr);
+  }
 
   // (a) top 64 groups, as composites (max key << 32) | ~group
   const uint64_t* chosen = sr.fast.sorted;
@@ -1062,6 +1164,7 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.status = status;
   a.decide = tab ? 1 : 0;
   a.q_after_wait = 1;
+  a.pen_logits = nullptr;
   const size_t smem = sizeof(smp::StageShared);
   static bool attr_set = false;
   if (!attr_set) {
@@ -1081,10 +1184,10 @@ bool sample_rows_supported(int vocab) {
   return (vocab + 31) / 32 <= smp::GI_MAX * smp::THREADS;
 }
 
-int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t* gmax,
+int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
                        uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
                        const ReqTable& tab, int4* dec, int32_t* status, bool q_after_wait,
-                       cudaStream_t stream) {
+                       float* pen_logits, cudaStream_t stream) {
   smp::SampleArgs a{};
   a.logits = logits;
   a.vocab = vocab;
@@ -1096,6 +1199,7 @@ int launch_sample_rows(const float* logits, int rows, int vocab, const uint32_t*
   a.status = status;
   a.decide = 1;
   a.q_after_wait = q_after_wait ? 1 : 0;
+  a.pen_logits = pen_logits;
   const size_t smem = sizeof(smp::RowsShared);
   static bool attr_set = false;
   if (!attr_set) {
