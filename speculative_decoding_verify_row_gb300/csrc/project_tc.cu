@@ -481,6 +481,22 @@ bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map for tensor stores: boxes of box_outer rows of
+// box_inner floats (box_inner * 4 == 128: one 128-byte swizzled row each);
+// parts of a box past the array are not written.
+bool encode_f32_box_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint32_t box_inner, uint32_t box_outer) {
+  if (!get_encoder()) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D fp32 tensor map over a row-major [outer][inner] array, tiles of
 // box_outer x box_inner elements, no swizzle; reads past the array are zero.
 bool encode_f32_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

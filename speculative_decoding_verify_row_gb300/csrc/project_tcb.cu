@@ -20,7 +20,11 @@
 //    on how many rows share the call (within this path).
 //  * Warp 0 feeds a 2-stage TMA ring (32 KB of weights, evict-first in L2,
 //    and 64 KB of plane tiles, evict-last, per stage), one thread of warp 1
-//    issues M128 N256 K16 MMAs, warps 2-5 drain TMEM into the logits.
+//    issues M128 N256 K16 MMAs, warps 2-5 drain TMEM into the logits.  The
+//    accumulator fills all of TMEM, so the next tile's MMAs wait for the
+//    drain: the drain therefore only moves TMEM through two 16 KB staging
+//    buffers in shared memory (128-byte swizzled rows) and tensor stores
+//    write the logits to global memory in the background.
 //  * Optionally the epilogue records, per row and per 32 vocabulary rows, the
 //    largest order key (the sampling stage's filter).
 //  * All waits are bounded (VR_DEV_TIMEOUT), as in the chain projection.
@@ -51,7 +55,9 @@ constexpr int A_TILE_BYTES = BM * BK * 2;                                  // 16
 constexpr int STAGE_BYTES = W_TILE_BYTES + NPLANE * MH * A_TILE_BYTES;     // 98304
 constexpr int TMEM_COLS = MH * BN;                                         // 512
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int OUT_COLS = 32;                                               // per staged box
+constexpr int OUT_BYTES = BM * OUT_COLS * 4;                               // 16384
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * OUT_BYTES + 1024 + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // kind::f16 instruction descriptor: D f32, A and B bf16, both K-major,
@@ -61,14 +67,17 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
 
 __global__ void __launch_bounds__(THREADS, 1)
     project_tcb_kernel(const __grid_constant__ CUtensorMap tm_w,
-                       const __grid_constant__ CUtensorMap tm_a, int hidden, int vocab,
-                       int rows_in_group, int row_base, float* __restrict__ logits,
+                       const __grid_constant__ CUtensorMap tm_a,
+                       const __grid_constant__ CUtensorMap tm_out,
+                       const __grid_constant__ CUtensorMap tm_out2, int staged, int hidden,
+                       int vocab, int rows_in_group, int row_base, float* __restrict__ logits,
                        float* __restrict__ logits2, int vec_ok, uint32_t* __restrict__ gmax,
                        int ngroups, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* out_stage = smem + STAGES * STAGE_BYTES;               // 2 x 16 KB, 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + 2 * OUT_BYTES);
   // barrier slots: full[STAGES], empty[STAGES], tmem_full, tmem_empty
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -200,6 +209,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool vec = vec_ok != 0;           // 16-byte aligned rows: float4 stores
+    const int et = threadIdx.x - 64;        // epilogue thread 0..127
+    int box = 0;                            // staged boxes issued so far
     uint32_t tph = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
       const bool okw = mbar_wait(tfull, tph, abort_flag, status);
@@ -226,7 +237,29 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             gmax[static_cast<size_t>(row_base + rl) * ngroups + (v0 >> 5)] = k;
           }
-          if (rl < rows_in_group) {
+          if (staged) {
+            // row rl's 32 values into the staging box (row quarter*32 + lane,
+            // 16-byte chunk k at position k ^ (row & 7)), then one tensor
+            // store per output; the buffer is reused two boxes later, after
+            // the store that read it
+            const int b = box & 1;
+            uint8_t* buf = out_stage + b * OUT_BYTES;
+            if (et == 0) bulk_wait_read<1>();
+            named_sync(1, 128);
+            const int srow = quarter * 32 + lane;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(buf + srow * 128 + ((k ^ (srow & 7)) << 4)) =
+                  make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            named_sync(1, 128);
+            if (et == 0) {
+              tma_store_2d(&tm_out, smem_u32(buf), v0, row_base + mh * BM);
+              if (logits2) tma_store_2d(&tm_out2, smem_u32(buf), v0, row_base + mh * BM);
+              bulk_commit();
+            }
+            ++box;
+          } else if (rl < rows_in_group) {
             if (vec && v0 + 32 <= vocab) {
 #pragma unroll
               for (int i = 0; i < 8; ++i)
@@ -253,6 +286,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  // the tensor stores issued by the epilogue have written their data
+  if (staged && threadIdx.x == 64) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -339,6 +374,12 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
   const int grid = std::min(n_tiles, g_tcb_sms);
   const int vec_ok = (vocab % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(logits2) % 16 == 0);
+  // the staged epilogue's tensor stores: fp32 boxes of 32 columns x 128 rows
+  // (row stride vocab * 4 must be a multiple of 16 bytes, bases 16-aligned)
+  CUtensorMap tm_out{}, tm_out2{};
+  int staged = vec_ok && encode_f32_box_sw128(&tm_out, logits, vocab, rows, tcb::OUT_COLS, tcb::BM);
+  if (staged && logits2)
+    staged = encode_f32_box_sw128(&tm_out2, logits2, vocab, rows, tcb::OUT_COLS, tcb::BM);
   for (int g = 0; g < groups; ++g) {
     CUtensorMap tm_a;
     if (!encode_bf16_tile(&tm_a, pl + static_cast<size_t>(g) * tcb::NPLANE * tcb::GROUP * hidden,
@@ -346,8 +387,9 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
       return VR_ERR_ARG;
     const int rg = std::min(tcb::GROUP, rows - g * tcb::GROUP);
     if (launch_pdl(tcb::project_tcb_kernel, dim3(grid), dim3(tcb::THREADS), tcb::SMEM_BYTES,
-                   stream, tm_w, tm_a, hidden, vocab, rg, g * tcb::GROUP, logits, logits2,
-                   vec_ok, gmax, (vocab + 31) / 32, status) != cudaSuccess)
+                   stream, tm_w, tm_a, tm_out, tm_out2, staged, hidden, vocab, rg,
+                   g * tcb::GROUP, logits, logits2, vec_ok, gmax, (vocab + 31) / 32,
+                   status) != cudaSuccess)
       return VR_ERR_CUDA;
   }
   return VR_OK;

@@ -991,7 +991,7 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
 //  (b) the chosen groups' entries at or above tau (at most 64 x 32) are
 //      gathered and their top 64 taken;
 //  (c) pool, policy, decisions and acceptance as in sample_kernel.
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     sample_rows_kernel(const __grid_constant__ SampleArgs a, const __grid_constant__ ReqTable tab,
                        uint32_t* __restrict__ gmax, int ngroups) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];

@@ -13,6 +13,8 @@ namespace vr {
 // projection
 bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                       uint32_t box_inner, uint32_t box_outer);
+bool encode_f32_box_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint32_t box_inner, uint32_t box_outer);
 size_t tcb_plane_bytes(int rows, int hidden);
 // gmax (nullable): [rows][ceil(vocab/32)] largest order key per 32 vocab rows
 // logits2 (nullable): a second buffer receiving the same logits
