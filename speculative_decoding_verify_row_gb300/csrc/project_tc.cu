@@ -15,10 +15,14 @@
 //    N = 96, K = 16) and the same K order whatever the row count: rows past
 //    R are zero columns.  Row r's bits therefore do not depend on R.
 //  * Each CTA (one per SM, persistent) walks units of two 128-row vocab
-//    tiles.  Per 64-wide K block, one thread of warp 0 streams the two W
-//    tiles (2 x 16 KB) through a 5-stage TMA ring together with the block's
-//    plane tile (96 x 64 bf16, in the 128-byte swizzled layout the MMA
-//    reads).  For up to 16 rows the planes are built in the kernel: the TMA
+//    tiles.  Per 64-wide K block, one thread of warp 0 streams the unit's
+//    256 x 64 W block (32 KB) through a 5-stage TMA ring together with the
+//    block's plane tile (96 x 64 bf16, in the 128-byte swizzled layout the
+//    MMA reads).  The W block is one 256-row box: the same bytes and
+//    shared-memory layout as two 128-row boxes with one TMA instruction
+//    (a TMA-only stream of these weights ran faster with the single box).
+//    In the last unit of an odd tile count its second half lies past the
+//    vocabulary and is zero-filled by the TMA; no MMA reads it.  For up to 16 rows the planes are built in the kernel: the TMA
 //    brings the group's fp32 activations for the block (R x 64) into the
 //    end of the plane tile and warp 6 splits them in place, so no separate
 //    pass runs before the projection.  For more rows one warp cannot keep
@@ -270,8 +274,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int last_fill_parity[STAGES];
       for (int i = 0; i < STAGES; ++i) last_fill_parity[i] = -1;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-        const int nmt = min(MT, n_mtiles - u * MT);
-        const uint32_t bytes = nmt * W_TILE_BYTES + (kFused ? 0 : B_TILE_BYTES);
+        // the full box always lands: rows past the vocabulary arrive as zeros
+        const uint32_t bytes = MT * W_TILE_BYTES + (kFused ? 0 : B_TILE_BYTES);
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) break;
           uint8_t* st = smem + s * STAGE_BYTES;
@@ -283,9 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(full_bar(s), bytes);
           if (!kFused)
             tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_x, kb * BK, 0, full_bar(s), pol_x);
-          for (int mt = 0; mt < nmt; ++mt)
-            tma_load_2d(smem_u32(st + mt * W_TILE_BYTES), &tm_w, kb * BK, (u * MT + mt) * BM,
-                        full_bar(s), pol_w);
+          tma_load_2d(smem_u32(st), &tm_w, kb * BK, u * MT * BM, full_bar(s), pol_w);
           last_fill_parity[s] = static_cast<int>(ph);
           if (++s == STAGES) {
             s = 0;
@@ -549,7 +551,8 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
       return VR_ERR_CUDA;
   }
   CUtensorMap tm_w;
-  if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::BM)) return VR_ERR_ARG;
+  // one 256-row box per unit and K block (both vocab tiles of the unit)
+  if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::MT * tc::BM)) return VR_ERR_ARG;
   const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
   const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
   const int grid = std::min(n_units, g_num_sms);
