@@ -301,12 +301,15 @@ VR_API int vr_verify_window_batched(const uint16_t* weight, const float* act, in
 /*
  * vr_verify_window with HOST inputs and outputs, for callers whose per-window
  * data lives on the host: act_h [rows][hidden], tokens_h, parent_h (or
- * NULL), q_ids_h/q_logits_h (or NULL), hist_h [hist_len] are host pointers
- * (pinned memory makes the copies asynchronous); the last
- * min(hist_len, VR_MAX_PENALTY_WINDOW) history tokens are copied.  weight,
- * logits and pen_logits are device pointers.  The call copies the inputs
- * into ws, runs the window, copies out_ids_h [rows], *out_accept_h and
- * *out_n_emitted_h back and SYNCHRONISES the stream before returning.
+ * NULL), q_ids_h/q_logits_h (or NULL), hist_h [hist_len] are host pointers;
+ * the last min(hist_len, VR_MAX_PENALTY_WINDOW) history tokens are used.
+ * weight, logits and pen_logits are device pointers.  The inputs go into ws:
+ * when every input buffer is pinned (page-locked, so mapped into the device's
+ * address space) a staging kernel reads them directly, otherwise they are
+ * copied.  Then the window runs; a pinned out_ids_h [rows] is written by the
+ * kernel, a pageable one copied back; *out_accept_h and *out_n_emitted_h
+ * are copied back and the call SYNCHRONISES the stream before returning (one
+ * wait per call).
  */
 VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
                           int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,
@@ -315,6 +318,32 @@ VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int
                           uint64_t seed, uint64_t position, float* logits, float* pen_logits,
                           int32_t* out_ids_h, int32_t* out_accept_h, int32_t* out_n_emitted_h,
                           void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * vr_verify_window_host without the wait, for a serving loop over independent
+ * windows that enqueues the next window before it reads the previous one.
+ * Inputs and arguments as in vr_verify_window_host.  The call stages the
+ * inputs into ws as vr_verify_window_host does, enqueues the window and
+ * returns.  out_h receives (2 + rows) int32: out_h[0] = accept,
+ * out_h[1] = n_emitted, out_h[2 .. 2 + n_emitted) = the emitted ids.
+ * Ownership and lifetime (all caller-owned):
+ *   - out_h should be pinned (page-locked) host memory: the acceptance writes
+ *     it directly (a pageable out_h gets one asynchronous copy); it is valid
+ *     only once the stream (or an event recorded after this call) has completed;
+ *   - pinned host inputs are read by the GPU after the call returns, so they
+ *     must stay unchanged until the stream has passed this call;
+ *   - windows enqueued on one stream with one ws run in order, each reading its
+ *     own inputs.
+ * Argument errors return before anything is enqueued; a device status is
+ * reported as for the other calls (vr_device_status).
+ */
+VR_API int vr_verify_window_host_async(const uint16_t* weight, const float* act_h, int rows,
+                                int hidden, int vocab, int path, const int32_t* tokens_h,
+                                const int32_t* parent_h, int n_nodes, const int32_t* q_ids_h,
+                                const float* q_logits_h, const int32_t* hist_h, int hist_len,
+                                const vr_policy* policy, uint64_t seed, uint64_t position,
+                                float* logits, float* pen_logits, int32_t* out_h, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Host-side draft proposal and window pricing.  These run on the CPU, take

@@ -116,6 +116,9 @@ _SIGNATURES = {
     "vr_verify_window_host": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I,
                                ctypes.POINTER(vr_policy), _U64, _U64, _P, _P, _P, _P, _P, _P,
                                _SZ, _P], _I),
+    "vr_verify_window_host_async": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I,
+                                     ctypes.POINTER(vr_policy), _U64, _U64, _P, _P, _P, _P,
+                                     _SZ, _P], _I),
     "vr_device_status": ([_P, ctypes.POINTER(ctypes.c_int32), _P], _I),
 }
 
@@ -353,8 +356,9 @@ def _host_ptr(a, dtype, name):
 def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
                        ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
                        pen_logits=None, path=VR_PATH_AUTO, stream=None):
-    """The window with host inputs and outputs (pinned host tensors make the
-    copies asynchronous).  Returns (accept, n_emitted); synchronises."""
+    """The window with host inputs and outputs (pinned host tensors are read
+    and written by the kernels directly, pageable ones copied).  Returns
+    (accept, n_emitted); synchronises."""
     V, H = weight.shape
     R = act_h.shape[0]
     n = R - 1
@@ -376,6 +380,32 @@ def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, 
                                        ctypes.byref(acc), ctypes.byref(ne), _ptr(ws), ws.numel(),
                                        _stream(stream, logits.device)), "vr_verify_window_host")
     return acc.value, ne.value
+
+
+def verify_window_host_async(weight, act_h, tokens_h, policy, seed, position, logits, out_h,
+                             ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
+                             pen_logits=None, path=VR_PATH_AUTO, stream=None):
+    """vr_verify_window_host_async: enqueues the window and one copy of
+    [accept, n_emitted, ids...] into out_h (pinned int32 [rows + 2]); returns
+    at once.  out_h is valid after the stream (or a later event) completes;
+    pinned inputs must stay unchanged until then."""
+    V, H = weight.shape
+    R = act_h.shape[0]
+    n = R - 1
+    _dev(weight, _WEIGHT_DTYPES, "weight")
+    _dev(logits, torch.float32, "logits", (R, V))
+    _dev(pen_logits, torch.float32, "pen_logits", (R, V))
+    if out_h.numel() < R + 2:
+        raise ValueError("out_h needs rows + 2 int32")
+    pol = policy.c()
+    _check(lib().vr_verify_window_host_async(
+        _ptr(weight), _host_ptr(act_h, torch.float32, "act_h"), R, H, V, path,
+        _host_ptr(tokens_h, torch.int32, "tokens_h"), _host_ptr(parent_h, torch.int32, "parent_h"),
+        n, _host_ptr(q_ids_h, torch.int32, "q_ids_h"),
+        _host_ptr(q_logits_h, torch.float32, "q_logits_h"), _host_ptr(hist_h, torch.int32, "hist_h"),
+        0 if hist_h is None else hist_h.numel(), ctypes.byref(pol), seed, position, _ptr(logits),
+        _ptr(pen_logits), _host_ptr(out_h, torch.int32, "out_h"), _ptr(ws), ws.numel(),
+        _stream(stream, logits.device)), "vr_verify_window_host_async")
 
 
 # ---------------------------------------------------------------------------

@@ -403,6 +403,97 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
   return sample_stages(tab, n_req, rows, vocab, target, gmax, any_active, any_q, ws, L, s);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The device address of a pinned (page-locked, device-mapped) host buffer,
+// or nullptr when the buffer is pageable (then it is copied instead).
+template <class T>
+T* mapped(T* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return static_cast<T*>(a.devicePointer);
+}
+
+// The host-buffer window: checks, the inputs into ws (read by the staging
+// kernel from pinned memory, else copied), then the window itself, whose
+// acceptance writes ids/accept/n to the given device-writable addresses.
+int window_host_enqueue(const uint16_t* weight, const float* act_h, int rows, int hidden,
+                        int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,
+                        int n_nodes, const int32_t* q_ids_h, const float* q_logits_h,
+                        const int32_t* hist_h, int hist_len, const vr_policy* policy,
+                        uint64_t seed, uint64_t position, float* logits, float* pen_logits,
+                        void* ws, size_t ws_bytes, cudaStream_t s, int32_t* ids_dst,
+                        int32_t* accept_dst, int32_t* n_dst) {
+  const Layout L = layout(rows, hidden, vocab);
+  const int h_keep = std::min(hist_len, VR_MAX_PENALTY_WINDOW);
+  const int32_t* hist_tail = h_keep > 0 ? hist_h + (hist_len - h_keep) : nullptr;
+  struct In {
+    const void* h;
+    size_t off, words;
+  };
+  const In in[kMaxStageSegs] = {
+      {act_h, L.st_act, static_cast<size_t>(rows) * hidden},
+      {n_nodes ? tokens_h : nullptr, L.st_tok, static_cast<size_t>(n_nodes)},
+      {parent_h, L.st_par, static_cast<size_t>(n_nodes)},
+      {q_ids_h, L.st_qid, static_cast<size_t>(n_nodes) * kQCand},
+      {q_logits_h, L.st_qlog, static_cast<size_t>(n_nodes) * kQCand},
+      {hist_tail, L.st_hist, static_cast<size_t>(h_keep)}};
+  StageSeg seg[kMaxStageSegs];
+  int nseg = 0;
+  bool all_mapped = true;
+  for (const In& x : in) {
+    if (!x.h || x.words == 0) continue;
+    const void* m = mapped(x.h);
+    if (!m) {
+      all_mapped = false;
+      break;
+    }
+    seg[nseg++] = {static_cast<const uint32_t*>(m), at<uint32_t>(ws, x.off),
+                   static_cast<uint32_t>(x.words)};
+  }
+  if (all_mapped) {
+    const int st = launch_stage_inputs(seg, nseg, s);
+    if (st != VR_OK) return st;
+  } else {
+    for (const In& x : in)
+      if (x.h && x.words &&
+          cudaMemcpyAsync(at<void>(ws, x.off), x.h, x.words * 4, cudaMemcpyHostToDevice, s) !=
+              cudaSuccess)
+        return VR_ERR_CUDA;
+  }
+  return window_device(weight, at<float>(ws, L.st_act), rows, hidden, vocab, path,
+                       at<int32_t>(ws, L.st_tok), parent_h ? at<int32_t>(ws, L.st_par) : nullptr,
+                       n_nodes, q_ids_h ? at<int32_t>(ws, L.st_qid) : nullptr,
+                       q_logits_h ? at<float>(ws, L.st_qlog) : nullptr, at<int32_t>(ws, L.st_hist),
+                       h_keep, *policy, seed, position, logits, pen_logits, ids_dst, accept_dst,
+                       n_dst, ws, L, s);
+}
+
+int check_host_window(const uint16_t* weight, const float* act_h, int rows, int hidden, int vocab,
+                      int path, const int32_t* tokens_h, int n_nodes, const int32_t* q_ids_h,
+                      const float* q_logits_h, const int32_t* hist_h, int hist_len,
+                      const vr_policy* policy, const float* logits, void* ws, size_t ws_bytes) {
+  int st = check_policy(policy);
+  if (st != VR_OK) return st;
+  if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
+  if (!weight || !act_h || !logits) return VR_ERR_ARG;
+  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH || !aligned16(weight)) return VR_ERR_ARG;
+  if ((st = check_window(rows, n_nodes, tokens_h, q_ids_h, q_logits_h, hist_h, hist_len)) != VR_OK)
+    return st;
+  return check_ws(ws, ws_bytes, rows, hidden, vocab);
+}
+
+}  // namespace
+
+extern "C" {
+
 int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
                           int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,
                           int n_nodes, const int32_t* q_ids_h, const float* q_logits_h,
@@ -410,46 +501,54 @@ int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, 
                           uint64_t seed, uint64_t position, float* logits, float* pen_logits,
                           int32_t* out_ids_h, int32_t* out_accept_h, int32_t* out_n_emitted_h,
                           void* ws, size_t ws_bytes, void* stream) {
-  int st = check_policy(policy);
+  if (!out_ids_h || !out_accept_h || !out_n_emitted_h) return VR_ERR_ARG;
+  int st = check_host_window(weight, act_h, rows, hidden, vocab, path, tokens_h, n_nodes, q_ids_h,
+                             q_logits_h, hist_h, hist_len, policy, logits, ws, ws_bytes);
   if (st != VR_OK) return st;
-  if ((st = check_shape(rows, hidden, vocab)) != VR_OK) return st;
-  if (!weight || !act_h || !logits || !out_ids_h || !out_accept_h || !out_n_emitted_h)
-    return VR_ERR_ARG;
-  if (path < VR_PATH_AUTO || path > VR_PATH_TC_BATCH || !aligned16(weight)) return VR_ERR_ARG;
-  if ((st = check_window(rows, n_nodes, tokens_h, q_ids_h, q_logits_h, hist_h, hist_len)) != VR_OK)
-    return st;
-  if ((st = check_ws(ws, ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
-  const Layout L = layout(rows, hidden, vocab);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int h_keep = std::min(hist_len, VR_MAX_PENALTY_WINDOW);
-  auto h2d = [&](size_t off, const void* src, size_t bytes) {
-    return bytes == 0 || cudaMemcpyAsync(at<void>(ws, off), src, bytes, cudaMemcpyHostToDevice, s) ==
-                             cudaSuccess;
-  };
-  if (!h2d(L.st_act, act_h, static_cast<size_t>(rows) * hidden * 4) ||
-      !h2d(L.st_tok, tokens_h, static_cast<size_t>(n_nodes) * 4) ||
-      (parent_h && !h2d(L.st_par, parent_h, static_cast<size_t>(n_nodes) * 4)) ||
-      (q_ids_h && !h2d(L.st_qid, q_ids_h, static_cast<size_t>(n_nodes) * kQCand * 4)) ||
-      (q_logits_h && !h2d(L.st_qlog, q_logits_h, static_cast<size_t>(n_nodes) * kQCand * 4)) ||
-      (h_keep > 0 && !h2d(L.st_hist, hist_h + (hist_len - h_keep), static_cast<size_t>(h_keep) * 4)))
-    return VR_ERR_CUDA;
-  int32_t* out = at<int32_t>(ws, L.st_out);
-  st = window_device(weight, at<float>(ws, L.st_act), rows, hidden, vocab, path,
-                     at<int32_t>(ws, L.st_tok), parent_h ? at<int32_t>(ws, L.st_par) : nullptr,
-                     n_nodes, q_ids_h ? at<int32_t>(ws, L.st_qid) : nullptr,
-                     q_logits_h ? at<float>(ws, L.st_qlog) : nullptr, at<int32_t>(ws, L.st_hist),
-                     h_keep, *policy, seed, position, logits, pen_logits, out + 2, out, out + 1,
-                     ws, L, s);
+  int32_t* out = at<int32_t>(ws, layout(rows, hidden, vocab).st_out);
+  // pinned id buffers are written by the kernel; otherwise staged and copied
+  int32_t* ids_dev = mapped(out_ids_h);
+  st = window_host_enqueue(weight, act_h, rows, hidden, vocab, path, tokens_h, parent_h, n_nodes,
+                           q_ids_h, q_logits_h, hist_h, hist_len, policy, seed, position, logits,
+                           pen_logits, ws, ws_bytes, s, ids_dev ? ids_dev : out + 2, out, out + 1);
   if (st != VR_OK) return st;
+  // accept and n may be pageable, so their copy is the last one enqueued:
+  // the call waits once
   int32_t head[2];
-  if (cudaMemcpyAsync(head, out, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(out_ids_h, out + 2, static_cast<size_t>(rows) * sizeof(int32_t),
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  if ((!ids_dev && cudaMemcpyAsync(out_ids_h, out + 2, static_cast<size_t>(rows) * sizeof(int32_t),
+                                   cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      cudaMemcpyAsync(head, out, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return VR_ERR_CUDA;
   *out_accept_h = head[0];
   *out_n_emitted_h = head[1];
   return VR_OK;
+}
+
+int vr_verify_window_host_async(const uint16_t* weight, const float* act_h, int rows, int hidden,
+                                int vocab, int path, const int32_t* tokens_h,
+                                const int32_t* parent_h, int n_nodes, const int32_t* q_ids_h,
+                                const float* q_logits_h, const int32_t* hist_h, int hist_len,
+                                const vr_policy* policy, uint64_t seed, uint64_t position,
+                                float* logits, float* pen_logits, int32_t* out_h, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (!out_h) return VR_ERR_ARG;
+  int st = check_host_window(weight, act_h, rows, hidden, vocab, path, tokens_h, n_nodes, q_ids_h,
+                             q_logits_h, hist_h, hist_len, policy, logits, ws, ws_bytes);
+  if (st != VR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // pinned out_h: the acceptance writes it directly; otherwise one copy
+  int32_t* dev = mapped(out_h);
+  int32_t* out = dev ? dev : at<int32_t>(ws, layout(rows, hidden, vocab).st_out);
+  st = window_host_enqueue(weight, act_h, rows, hidden, vocab, path, tokens_h, parent_h, n_nodes,
+                           q_ids_h, q_logits_h, hist_h, hist_len, policy, seed, position, logits,
+                           pen_logits, ws, ws_bytes, s, out + 2, out, out + 1);
+  if (st != VR_OK || dev) return st;
+  return cudaMemcpyAsync(out_h, out, static_cast<size_t>(2 + rows) * sizeof(int32_t),
+                         cudaMemcpyDeviceToHost, s) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
 }
 
 int vr_device_status(void* ws, int32_t* out_status, void* stream) {

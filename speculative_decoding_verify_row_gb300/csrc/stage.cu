@@ -1,0 +1,85 @@
+// Staging of a window's host inputs by a kernel, for the host-buffer entry
+// points: the inputs live in pinned (page-locked, device-mapped) host memory
+// and are read by the GPU directly, before the kernel waits for its
+// predecessor, so the host-link latency overlaps the previous window; after
+// the wait the words are stored into the workspace.  This replaces one
+// host-to-device copy per input, each of which would serialise on the stream
+// and keep the projection from launching early.
+#include "vr_common.cuh"
+#include "vr_kernels.h"
+
+namespace vr {
+namespace {
+
+constexpr int kStageThreads = 256;
+constexpr int kStagePerThread = 4;      // words held in registers per thread
+
+struct StageArgs {
+  StageSeg seg[kMaxStageSegs];
+  uint32_t end[kMaxStageSegs];          // running word counts
+  int nseg;
+};
+
+__device__ __forceinline__ int seg_of(const StageArgs& a, uint32_t w) {
+  int s = 0;
+  while (s + 1 < a.nseg && w >= a.end[s]) ++s;
+  return s;
+}
+
+__global__ void __launch_bounds__(kStageThreads)
+    stage_inputs_kernel(const __grid_constant__ StageArgs a) {
+  const uint32_t total = a.end[a.nseg - 1];
+  const uint32_t base = blockIdx.x * (kStageThreads * kStagePerThread) + threadIdx.x;
+  uint32_t v[kStagePerThread];
+  // host reads first: nothing before this kernel writes the host buffers
+#pragma unroll
+  for (int i = 0; i < kStagePerThread; ++i) {
+    const uint32_t w = base + i * kStageThreads;
+    v[i] = 0u;
+    if (w < total) {
+      const int s = seg_of(a, w);
+      const uint32_t off = w - (s ? a.end[s - 1] : 0u);
+      v[i] = a.seg[s].src[off];
+    }
+  }
+  // the workspace may still be read by the previous window's kernels
+  pdl_wait();
+  // this kernel starts a window: dependents launch once it is past its wait
+  pdl_trigger();
+#pragma unroll
+  for (int i = 0; i < kStagePerThread; ++i) {
+    const uint32_t w = base + i * kStageThreads;
+    if (w < total) {
+      const int s = seg_of(a, w);
+      const uint32_t off = w - (s ? a.end[s - 1] : 0u);
+      a.seg[s].dst[off] = v[i];
+    }
+  }
+}
+
+}  // namespace
+
+int launch_stage_inputs(const StageSeg* segs, int nseg, cudaStream_t stream) {
+  if (nseg < 1 || nseg > kMaxStageSegs) return VR_ERR_ARG;
+  StageArgs a{};
+  uint64_t total = 0;
+  int n = 0;
+  for (int i = 0; i < nseg; ++i) {
+    if (segs[i].words == 0) continue;
+    total += segs[i].words;
+    a.seg[n] = segs[i];
+    a.end[n] = static_cast<uint32_t>(total);
+    ++n;
+  }
+  if (n == 0) return VR_OK;
+  if (total > 0xffffffffull - kStageThreads * kStagePerThread) return VR_ERR_ARG;
+  a.nseg = n;
+  const uint32_t per_cta = kStageThreads * kStagePerThread;
+  const uint32_t grid = static_cast<uint32_t>((total + per_cta - 1) / per_cta);
+  return launch_pdl(stage_inputs_kernel, dim3(grid), dim3(kStageThreads), 0, stream, a) ==
+                 cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
+}  // namespace vr

@@ -10,6 +10,16 @@
 
 namespace vr {
 
+// host inputs -> workspace by a kernel that reads device-mapped pinned host
+// memory (src: device addresses of pinned host buffers; dst: workspace)
+constexpr int kMaxStageSegs = 6;
+struct StageSeg {
+  const uint32_t* src;
+  uint32_t* dst;
+  uint32_t words;
+};
+int launch_stage_inputs(const StageSeg* segs, int nseg, cudaStream_t stream);
+
 // projection
 bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                       uint32_t box_inner, uint32_t box_outer);

@@ -311,13 +311,20 @@ def test_multi_window_history():
             assert hist[len(hist) - len(emitted):] == emitted
 
 
-def test_host_entry_point_matches_device_entry_point(big_weights_4096):
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_entry_point_matches_device_entry_point(big_weights_4096, pinned):
+    """Pinned host buffers are read and written by the kernels through their
+    mapped addresses; pageable ones go through copies.  Both equal the
+    device entry point."""
     bw = big_weights_4096
     pol = ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95, presence=1.5, window=64)
     A, L64, q_ids, q_log, drafts = chain_inputs(bw, 3, 77)
     hist = synth.zipf_history(4096, 151936, seed=77)
     win = run_window(bw.dev, A, drafts, pol, 77, 4096, q_ids=q_ids, q_log=q_log, hist=hist)
-    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    if pinned:
+        pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    else:
+        pin = lambda x: torch.from_numpy(np.ascontiguousarray(x).copy())
     logits = torch.empty((4, 151936), dtype=torch.float32, device="cuda")
     out = pin(np.full(4, -7, np.int32))
     ws = vb.workspace(4, 4096, 151936)
@@ -327,6 +334,36 @@ def test_host_entry_point_matches_device_entry_point(big_weights_4096):
     assert list(out.numpy()[:n]) == list(win["ids"][:n])
     # no separate penalised buffer was given, so the penalties went in place
     assert torch.equal(logits.view(torch.int32), win["pen"].view(torch.int32))
+
+
+def test_async_host_entry_point_pipelined(big_weights_4096):
+    """Several host-buffer windows enqueued back to back without waiting, each
+    read after its event: every one equals the same window run alone."""
+    bw = big_weights_4096
+    pol = ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95)
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    logits = torch.empty((4, 151936), dtype=torch.float32, device="cuda")
+    ws = vb.workspace(4, 4096, 151936)
+    stream = torch.cuda.current_stream()
+    cases, pending = [], []
+    for w in range(4):
+        A, L64, q_ids, q_log, drafts = chain_inputs(bw, 3, 300 + w)
+        cases.append((A, q_ids, q_log, drafts))
+        h = (pin(A), pin(drafts), pin(q_ids), pin(q_log))
+        # the last window's result goes to pageable memory: one copy instead
+        out = pin(np.full(6, -7, np.int32)) if w < 3 else torch.full((6,), -7, dtype=torch.int32)
+        vb.verify_window_host_async(bw.dev, h[0], h[1], bpol(pol), 300 + w, 4096, logits, out, ws,
+                                    q_ids_h=h[2], q_logits_h=h[3], stream=stream)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        pending.append((ev, out, h))
+    for w, (ev, out, _) in enumerate(pending):
+        ev.synchronize()
+        A, q_ids, q_log, drafts = cases[w]
+        win = run_window(bw.dev, A, drafts, pol, 300 + w, 4096, q_ids=q_ids, q_log=q_log)
+        got = out.numpy()
+        assert (int(got[0]), int(got[1])) == (win["accept"], win["n"])
+        assert list(got[2:2 + win["n"]]) == list(win["ids"][:win["n"]])
 
 
 @pytest.mark.parametrize("shape", ["chain", "tree_greedy", "tree_sampled"])
