@@ -345,6 +345,20 @@ VR_API int vr_verify_window_host_async(const uint16_t* weight, const float* act_
                                 float* logits, float* pen_logits, int32_t* out_h, void* ws,
                                 size_t ws_bytes, void* stream);
 
+/*
+ * The candidate pools of the last window (vr_verify_window, its host-buffer
+ * variants or vr_verify_window_batched) enqueued with this workspace, copied
+ * on `stream` into ids [rows][64] int32 and vals [rows][64] float32 (device
+ * pointers, caller-owned).  Each row is the top 64 of that row's logits
+ * after its penalties, in pool order ("Speculative decoding on RDNA" §03:
+ * value descending, token id ascending, NaN lowest); entries past the
+ * vocabulary are id -1.  rows, hidden and vocab are those of that call
+ * (the batched call: its total rows).  Argument errors return before
+ * anything is enqueued.
+ */
+VR_API int vr_window_pools(const void* ws, size_t ws_bytes, int rows, int hidden, int vocab,
+                    int32_t* ids, float* vals, void* stream);
+
 /* ------------------------------------------------------------------------
  * Host-side draft proposal and window pricing.  These run on the CPU, take
  * HOST pointers only, enqueue nothing and need no GPU.

@@ -119,6 +119,7 @@ _SIGNATURES = {
     "vr_verify_window_host_async": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I,
                                      ctypes.POINTER(vr_policy), _U64, _U64, _P, _P, _P, _P,
                                      _SZ, _P], _I),
+    "vr_window_pools": ([_P, _SZ, _I, _I, _I, _P, _P, _P], _I),
     "vr_device_status": ([_P, ctypes.POINTER(ctypes.c_int32), _P], _I),
 }
 
@@ -406,6 +407,15 @@ def verify_window_host_async(weight, act_h, tokens_h, policy, seed, position, lo
         0 if hist_h is None else hist_h.numel(), ctypes.byref(pol), seed, position, _ptr(logits),
         _ptr(pen_logits), _host_ptr(out_h, torch.int32, "out_h"), _ptr(ws), ws.numel(),
         _stream(stream, logits.device)), "vr_verify_window_host_async")
+
+
+def window_pools(ws, rows, hidden, vocab, ids, vals, stream=None):
+    """vr_window_pools: the last window's pools (ids int32 [rows][64], vals
+    float32 [rows][64], device tensors) from the workspace it ran with."""
+    _dev(ids, torch.int32, "ids", (rows, 64))
+    _dev(vals, torch.float32, "vals", (rows, 64))
+    _check(lib().vr_window_pools(_ptr(ws), ws.numel(), rows, hidden, vocab, _ptr(ids), _ptr(vals),
+                                 _stream(stream, ids.device)), "vr_window_pools")
 
 
 # ---------------------------------------------------------------------------

@@ -551,6 +551,24 @@ int vr_verify_window_host_async(const uint16_t* weight, const float* act_h, int 
              : VR_ERR_CUDA;
 }
 
+int vr_window_pools(const void* ws, size_t ws_bytes, int rows, int hidden, int vocab, int32_t* ids,
+                    float* vals, void* stream) {
+  if (!ids || !vals) return VR_ERR_ARG;
+  int st = check_shape(rows, hidden, vocab);
+  if (st != VR_OK) return st;
+  if ((st = check_ws(const_cast<void*>(ws), ws_bytes, rows, hidden, vocab)) != VR_OK) return st;
+  const Layout L = layout(rows, hidden, vocab);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(rows) * kPool * 4;
+  void* w = const_cast<void*>(ws);
+  return cudaMemcpyAsync(ids, at<int32_t>(w, L.pool_ids), bytes, cudaMemcpyDeviceToDevice, s) ==
+                     cudaSuccess &&
+                 cudaMemcpyAsync(vals, at<float>(w, L.pool_vals), bytes, cudaMemcpyDeviceToDevice,
+                                 s) == cudaSuccess
+             ? VR_OK
+             : VR_ERR_CUDA;
+}
+
 int vr_device_status(void* ws, int32_t* out_status, void* stream) {
   if (!ws || !out_status) return VR_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -987,7 +987,8 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
 // vocabulary rows) were recorded by the projection: one CTA per row.
 //  (a) the row's 64 groups with the largest maxima (ties: lower group index),
 //      tau = the maximum of the 64th: at least 64 entries reach tau, and every
-//      entry of the row's top 64 lies in those groups at or above tau;
+//      entry of the row's top 64 lies in those groups at or above tau (a row
+//      of fewer than 64 groups takes all of them with tau = the lowest key);
 //  (b) the chosen groups' entries at or above tau (at most 64 x 32) are
 //      gathered and their top 64 taken;
 //  (c) pool, policy, decisions and acceptance as in sample_kernel.
@@ -1041,7 +1042,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
   const int nchosen = ngroups < kPool ? ngroups : kPool;
-  const uint32_t tau = static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
+  // 64 chosen groups hold at least 64 entries at or above the 64th group
+  // maximum; with fewer groups every entry of every group is a candidate
+  const uint32_t tau = ngroups < kPool ? 0u : static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
   if (tid == 0) sr.ccount = 0;
   __syncthreads();
 

@@ -52,7 +52,7 @@ def run_window(wd, act, tokens, pol, seed, position, parent=None, q_ids=None, q_
     assert vb.device_status(ws) == 0
     penalised = pen if (pen is not None and ov.penalties_active(pol)) else logits
     return dict(logits=logits, pen=penalised, ids=out.cpu().numpy(), accept=int(acc.item()),
-                n=int(ne.item()))
+                n=int(ne.item()), ws=ws)
 
 
 def gpu_sample(pen_np, tokens, pol, seed, position, parent=None, q_ids=None, q_pen=None):
@@ -398,3 +398,89 @@ def test_ngram_drafted_windows_full_size(big_weights_4096, shape):
         check_window(win, L64, tokens, pol, s, len(ctx), parent=parent, hist=ctx, stats=stats,
                      logit_cols=cols_sample(V, 900 + s))
     assert stats["compared"] >= 2
+
+
+def _bf16_column(values):
+    """float32 values (NaN allowed) -> bf16 bits (finite values rounded to
+    nearest even, NaN as the quiet NaN 0x7fc0)."""
+    v = np.asarray(values, np.float32)
+    bits = synth.f32_to_bf16_bits(np.where(np.isnan(v), 0.0, v).astype(np.float32))
+    bits[np.isnan(v)] = 0x7FC0
+    return bits
+
+
+def _crafted_rows(V, seed):
+    """Four logit rows that stress the group-maxima selection: all entries
+    equal (every group ties, 2048 candidates); a top value shared by a block
+    of 40 ids and ~30 scattered ids; four distinct values with NaNs; distinct
+    values with 20 % NaN, a whole NaN group and a top cluster in bf16 ties."""
+    rng = np.random.default_rng(seed)
+    rows = np.empty((4, V), np.float32)
+    rows[0] = 0.5
+    r1 = rng.standard_normal(V).astype(np.float32)
+    r1[rng.random(V) < 30.0 / V] = 3.0
+    r1[64:104] = 3.0
+    rows[1] = r1
+    r2 = rng.choice(np.array([-1.0, 0.0, 0.25, 1.0], np.float32), V, p=[0.3, 0.2, 0.25, 0.25])
+    r2[rng.random(V) < 0.05] = np.nan
+    rows[2] = r2
+    r3 = rng.standard_normal(V).astype(np.float32)
+    r3[rng.random(V) < 0.2] = np.nan
+    r3[32:96] = 5.0 + 0.01 * np.arange(64, dtype=np.float32)[:len(r3[32:96])]
+    r3[160:192] = np.nan
+    rows[3] = r3
+    return rows
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+@pytest.mark.parametrize("V", [100, 2047, 5000, 151936, 163840, 163841])
+@pytest.mark.parametrize("mode", ["greedy", "sampled", "penalised"])
+def test_row_pools_on_crafted_logits(V, mode, path):
+    """With one-hot activations the projection returns chosen bf16 values
+    exactly (logits[r][v] = W[v][r], NaN where W[v] holds a NaN), so the
+    pool selection of the window
+    path (group maxima from the projection epilogue, then the row kernel; or
+    the segment select past 5120 groups) meets ties across groups, gathers
+    past its fast capacity, NaN and vocabularies with fewer than 64 groups.
+    Pools must equal the oracle's pool of the same rows bit for bit, and the
+    window's result the oracle's window on them."""
+    H, R = 64, 4
+    rows = _crafted_rows(V, seed=V)
+    rng = np.random.default_rng(V + 1)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.1))
+    for r in range(R):
+        W[:, r] = _bf16_column(rows[r])
+    A = np.zeros((R, H), np.float32)
+    A[np.arange(R), np.arange(R)] = 1.0
+    # W[v][r] exactly, except that a NaN anywhere in W[v] reaches every row
+    # (NaN x 0); the fp64 oracle projection is exact here
+    exact = ov.project(W, A).astype(np.float32)
+    if mode == "greedy":
+        pol = ov.Policy(temperature=0.0)
+    elif mode == "sampled":
+        pol = ov.Policy(temperature=0.8, top_k=0, min_p=0.0, top_p=1.0)
+    else:
+        pol = ov.Policy(temperature=0.8, top_k=0, min_p=0.0, top_p=1.0, presence=0.75,
+                        frequency=0.25, window=64)
+    argmax = [int(ov.target_pool(exact[r])[0][0]) for r in range(R)]
+    drafts = np.array([argmax[0], argmax[1], int(rng.integers(0, V))], np.int32)
+    hist = np.array([argmax[0], 64, 65, 32, 33, 7] * 3, np.int32) % V if mode == "penalised" else None
+    win = run_window(dev_weight(W), A, drafts, pol, 5, 100, hist=hist, path=path)
+    assert same_bits_f32(win["logits"].cpu().numpy(), exact)
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    vb.window_pools(win["ws"], R, H, V, ids, vals)
+    torch.cuda.synchronize()
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    pen = win["pen"].cpu().numpy()
+    n = min(64, V)
+    for r in range(R):
+        want_ids, want_vals = ov.target_pool(pen[r])
+        assert np.array_equal(ids[r, :n], want_ids), (mode, V, r)
+        assert same_bits_f32(vals[r, :n], want_vals), (mode, V, r)
+        assert (ids[r, n:] == -1).all()
+    ref = ov.verify_window(win["logits"].cpu().numpy(), drafts, hist=() if hist is None else hist,
+                           pol=pol, seed=5, position=100)
+    if mode == "penalised":
+        assert same_bits_f32(pen, ref.pen_logits)
+    assert list(win["ids"][:win["n"]]) == ref.emitted and win["accept"] == ref.accept
