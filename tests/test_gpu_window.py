@@ -433,7 +433,7 @@ def _crafted_rows(V, seed):
 
 
 @pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
-@pytest.mark.parametrize("V", [100, 2047, 5000, 151936, 163840, 163841])
+@pytest.mark.parametrize("V", [1, 33, 100, 2047, 5000, 151936, 163840, 163841])
 @pytest.mark.parametrize("mode", ["greedy", "sampled", "penalised"])
 def test_row_pools_on_crafted_logits(V, mode, path):
     """With one-hot activations the projection returns chosen bf16 values
