@@ -20,6 +20,12 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work
  *     is enqueued asynchronously; outputs are valid once the stream has
  *     reached that point.  No entry point synchronises unless it says so.
+ *   - Kernels are launched with programmatic dependent launch.  Every input
+ *     except the weights is read only after the kernel before it on the
+ *     stream has completed.  The tensor-core projection requests its first
+ *     weight blocks as soon as it starts, which is before that kernel ends
+ *     when the kernel lets dependents launch early (griddepcontrol.
+ *     launch_dependents); a kernel that does so must not write the weights.
  *   - Return value: VR_OK or a negative VR_ERR_* code.  Argument errors are
  *     detected on the host before anything is enqueued.  Errors that depend
  *     on device-resident data (a token outside the vocabulary, a parent

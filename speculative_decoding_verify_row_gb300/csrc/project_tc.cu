@@ -254,8 +254,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // the prologue above overlaps the previous kernel; from here on the
-  // activations and the logits buffer are touched, so wait for it to complete
+  // No kernel of a window writes the weights, so the producer requests the
+  // first stages' weight blocks before the wait: the weight stream starts
+  // while the previous kernel finishes.  The stages complete only after the
+  // wait, when the producer arrives on them (with the activations' bytes).
+  int prefilled = 0;
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol_w = l2_policy_evict_first();
+    const int my_units =
+        static_cast<int>(blockIdx.x) < n_units ? (n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    prefilled = min(STAGES, my_units * n_kb);
+    for (int i = 0; i < prefilled; ++i) {
+      const int u = blockIdx.x + (i / n_kb) * gridDim.x;
+      mbar_add_tx(full_bar(i), MT * W_TILE_BYTES);
+      tma_load_2d(smem_u32(smem + i * STAGE_BYTES), &tm_w, (i % n_kb) * BK, u * MT * BM,
+                  full_bar(i), pol_w);
+    }
+  }
+  // from here on the activations and the logits buffer are touched, so wait
+  // for the previous kernel to complete
   pdl_wait();
   // a window starts with this kernel: its dependents may launch only now,
   // once every kernel before the window is complete, because the later
@@ -271,12 +288,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int stg_off = B_TILE_BYTES - rows_in_group * BK * 4;
       int s = 0;
       uint32_t ph = 0;
+      int it = 0;
       int last_fill_parity[STAGES];
-      for (int i = 0; i < STAGES; ++i) last_fill_parity[i] = -1;
+      for (int i = 0; i < STAGES; ++i) last_fill_parity[i] = i < prefilled ? 0 : -1;
       for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-        // the full box always lands: rows past the vocabulary arrive as zeros
-        const uint32_t bytes = MT * W_TILE_BYTES + (kFused ? 0 : B_TILE_BYTES);
-        for (int kb = 0; kb < n_kb; ++kb) {
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) break;
           uint8_t* st = smem + s * STAGE_BYTES;
           if (kFused) {
@@ -284,10 +300,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(smem_u32(st + MT * W_TILE_BYTES + stg_off), &tm_x, kb * BK, row_base,
                         afull_bar(s), pol_x);
           }
-          mbar_expect_tx(full_bar(s), bytes);
+          // the full box always lands: rows past the vocabulary arrive as
+          // zeros; a prefilled stage's weight bytes were expected already
+          const bool pre = it < prefilled;
+          mbar_expect_tx(full_bar(s), (pre ? 0u : static_cast<uint32_t>(MT * W_TILE_BYTES)) +
+                                          (kFused ? 0u : static_cast<uint32_t>(B_TILE_BYTES)));
           if (!kFused)
             tma_load_2d(smem_u32(st + MT * W_TILE_BYTES), &tm_x, kb * BK, 0, full_bar(s), pol_x);
-          tma_load_2d(smem_u32(st), &tm_w, kb * BK, u * MT * BM, full_bar(s), pol_w);
+          if (!pre) tma_load_2d(smem_u32(st), &tm_w, kb * BK, u * MT * BM, full_bar(s), pol_w);
           last_fill_parity[s] = static_cast<int>(ph);
           if (++s == STAGES) {
             s = 0;
