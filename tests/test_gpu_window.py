@@ -484,3 +484,94 @@ def test_row_pools_on_crafted_logits(V, mode, path):
     if mode == "penalised":
         assert same_bits_f32(pen, ref.pen_logits)
     assert list(win["ids"][:win["n"]]) == ref.emitted and win["accept"] == ref.accept
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+@pytest.mark.parametrize("V", [1000, 151936])
+def test_batched_requests_on_crafted_logits(V, path):
+    """One batched call over eight requests of different shapes and policies
+    (chain of 4 rows, a single row, a 5-row tree, chain of 8 rows; greedy,
+    sampled against draft candidates, sampled against the point mass,
+    penalised) on crafted logits (one-hot activations: row r reads weight
+    column r % 64, each column a tie/NaN pattern or random bf16 values).
+    Every row's pool and every request's result must equal the oracle's on
+    the GPU's own logits."""
+    H = 64
+    rng = np.random.default_rng(V + 7)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.1))
+    base = _crafted_rows(V, seed=V + 3)
+    for c in range(H):
+        if c % 4 == 0 and c // 4 < 4:
+            W[:, c] = _bf16_column(base[c // 4])
+        elif c % 3 == 0:
+            # few distinct values: ties everywhere
+            W[:, c] = _bf16_column(rng.choice(np.array([-0.5, 0.5, 1.0, 2.0], np.float32), V))
+    shapes = [(3, None), (0, None), (4, [-1, 0, -1, 2]), (7, None)] * 2
+    pols = [ov.Policy(temperature=0.0),
+            ov.Policy(temperature=0.8, top_k=0, min_p=0.0, top_p=1.0),
+            ov.Policy(temperature=0.7, top_k=20, min_p=0.05, top_p=0.9),
+            ov.Policy(temperature=0.8, top_k=0, presence=0.75, frequency=0.25, window=64),
+            ov.Policy(temperature=0.0, presence=1.5, window=16),
+            ov.Policy(temperature=1.1, top_k=5, min_p=0.0, top_p=0.8),
+            ov.Policy(temperature=0.5, top_k=64, min_p=0.2, top_p=1.0, repeat=1.3, window=8),
+            ov.Policy(temperature=0.9, top_k=-1, min_p=0.0, top_p=0.95)]
+    rows_of = []
+    r0 = 0
+    for n, _ in shapes:
+        rows_of.append(list(range(r0, r0 + n + 1)))
+        r0 += n + 1
+    R = r0
+    A = np.zeros((R, H), np.float32)
+    A[np.arange(R), np.arange(R) % H] = 1.0
+    exact = ov.project(W, A).astype(np.float32)
+    reqs, keep, specs = [], [], []
+    for b, ((n, parent), pol) in enumerate(zip(shapes, pols)):
+        par = ov.chain_parents(n) if parent is None else parent
+        am = [int(ov.target_pool(exact[rows_of[b][0] + (0 if p < 0 else 1 + p)])[0][0]) for p in par]
+        tokens = np.array([am[j] if j % 2 == 0 else int(rng.integers(0, V)) for j in range(n)],
+                          np.int32)
+        with_q = parent is None and n > 0 and b % 2 == 1 and pol.temperature > 0
+        q_ids = q_log = None
+        if with_q:
+            q_ids = rng.integers(0, V, (n, 8)).astype(np.int32)
+            q_ids[:, 0] = tokens
+            q_log = rng.standard_normal((n, 8)).astype(np.float32)
+        hist = (rng.integers(0, V, 40).astype(np.int32) if ov.penalties_active(pol) else None)
+        t = dict(tok=dev(tokens) if n else None,
+                 par=None if parent is None else dev(np.array(parent, np.int32)),
+                 q=None if q_ids is None else dev(q_ids), ql=None if q_log is None else dev(q_log),
+                 h=None if hist is None else dev(hist),
+                 out=torch.full((n + 1,), -7, dtype=torch.int32, device="cuda"),
+                 acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                 n=torch.zeros(1, dtype=torch.int32, device="cuda"))
+        keep.append(t)
+        specs.append((tokens, parent, q_ids, q_log, hist, pol))
+        reqs.append(vb.make_request(n, t["tok"], bpol(pol), 40 + b, 300 + b, t["out"], t["acc"],
+                                    t["n"], parent=t["par"], q_ids=t["q"], q_logits=t["ql"],
+                                    hist=t["h"]))
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(logits)
+    ws = vb.workspace(R, H, V)
+    vb.verify_window_batched(dev_weight(W), dev(A), reqs, logits, ws, pen_logits=pen, path=path)
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    vb.window_pools(ws, R, H, V, ids, vals)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    g_logits = logits.cpu().numpy()
+    assert same_bits_f32(g_logits, exact)
+    ids, vals, g_pen = ids.cpu().numpy(), vals.cpu().numpy(), pen.cpu().numpy()
+    for b, (tokens, parent, q_ids, q_log, hist, pol) in enumerate(specs):
+        rs = rows_of[b]
+        ref = ov.verify_window(g_logits[rs], tokens, parent, q_ids, q_log,
+                               () if hist is None else hist, pol, 40 + b, 300 + b)
+        rows_pen = g_pen[rs] if ov.penalties_active(pol) else g_logits[rs]
+        if ov.penalties_active(pol):
+            assert same_bits_f32(rows_pen, ref.pen_logits), b
+        for i, r in enumerate(rs):
+            want_ids, want_vals = ov.target_pool(rows_pen[i])
+            assert np.array_equal(ids[r, :len(want_ids)], want_ids), (b, i)
+            assert same_bits_f32(vals[r, :len(want_ids)], want_vals), (b, i)
+        n_em = int(keep[b]["n"].item())
+        assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
+        assert int(keep[b]["acc"].item()) == ref.accept, b
