@@ -432,16 +432,17 @@ def _crafted_rows(V, seed):
     return rows
 
 
-@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH, vb.VR_PATH_FFMA])
 @pytest.mark.parametrize("V", [1, 33, 100, 2047, 5000, 151936, 163840, 163841])
 @pytest.mark.parametrize("mode", ["greedy", "sampled", "penalised"])
 def test_row_pools_on_crafted_logits(V, mode, path):
     """With one-hot activations the projection returns chosen bf16 values
     exactly (logits[r][v] = W[v][r], NaN where W[v] holds a NaN), so the
     pool selection of the window
-    path (group maxima from the projection epilogue, then the row kernel; or
-    the segment select past 5120 groups) meets ties across groups, gathers
-    past its fast capacity, NaN and vocabularies with fewer than 64 groups.
+    path (group maxima from the projection epilogue, then the row kernel; the
+    segment select and its merge past 5120 groups and on the CUDA-core path)
+    meets ties across groups, gathers past its fast capacity, NaN and
+    vocabularies with fewer than 64 groups.
     Pools must equal the oracle's pool of the same rows bit for bit, and the
     window's result the oracle's window on them."""
     H, R = 64, 4
