@@ -610,9 +610,7 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShar
       qid[s2] = s2 < qm ? rs.qid[s2] : -1;
       qp[s2] = s2 < qm ? rs.qp[s2] : 0.0f;
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int jj = lane + 32 * h;
+    auto residual_entry = [&](int jj) {
       const int32_t id = rs.ids[jj];
       const float pj = __fdiv_rn(rs.e[jj], S);
       float qj = 0.0f;
@@ -622,7 +620,11 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShar
       const float d = __fsub_rn(pj, qj);
       rs.r[jj] = (jj < m && d > 0.0f) ? d : 0.0f;
       if (jj < m && id == xd) px = pj;
-    }
+    };
+    residual_entry(lane);
+    // the upper half only when more than 32 entries are kept (r past m is
+    // never read)
+    if (m > 32) residual_entry(lane + 32);
     // pool ids are distinct: at most one lane holds p(x)
     for (int o = 16; o >= 1; o >>= 1) {
       const float other = __shfl_xor_sync(0xffffffffu, px, o);

@@ -202,7 +202,8 @@ __device__ __forceinline__ int warp_first(int m, Pred pred) {
 // running sums c[j] = w_0 + ... + w_j for j < n <= N, sequential, by one
 // lane; w and c are 16-byte aligned arrays of at least N floats.  All N
 // weights are read first (no load waits inside the chain of additions);
-// entries past n count as zero, so c[j] for j >= n repeats c[n - 1].
+// entries past n count as zero, so c[j] for n <= j < N repeats c[n - 1];
+// c past N is not written.
 template <int N>
 __device__ __forceinline__ void running_sums_n(const float* w, float* c, int n) {
   float v[N];
@@ -231,8 +232,13 @@ __device__ __forceinline__ void running_sums_n(const float* w, float* c, int n) 
 }
 
 __device__ __forceinline__ void running_sums(const float* w, float* c, int n) {
+  // the shortest chain of additions that covers n (c past it is not read)
   if (n <= 8)
     running_sums_n<8>(w, c, n);
+  else if (n <= 16)
+    running_sums_n<16>(w, c, n);
+  else if (n <= 32)
+    running_sums_n<32>(w, c, n);
   else
     running_sums_n<64>(w, c, n);
 }
