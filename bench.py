@@ -275,6 +275,30 @@ def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
                          q_logits=w["ql"], hist=w["h"], pen_logits=pen, stream=stream)
     t = _event_time(torch, stream, pen_window, n_steps)
     out["penalised_chain_k8"] = {"windows_per_s": 1.0 / t, "us_per_window": 1e6 * t, "rows": R}
+    # the same windows through the stage entry points (projection, penalty
+    # prepass, pool + policy + acceptance), events between the stages; the
+    # fused call applies the penalties inside its row sampling kernel instead
+    n_st = min(n_steps, 200)
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_st)]
+    qpen = torch.empty((k, 8), dtype=torch.float32, device=dev)
+    for i in range(n_st):
+        w = wins[i % nwin]
+        qpen.copy_(w["ql"])
+        st_ev[i][0].record(stream)
+        vb.verify_project(wd, w["a"], lg, ws, stream=stream)
+        st_ev[i][1].record(stream)
+        vb.verify_penalize(lg, w["d"], w["h"], pol, ws, q_ids=w["q"], q_logits=qpen, stream=stream)
+        st_ev[i][2].record(stream)
+        vb.verify_sample_accept(lg, w["d"], pol, i, 4096, o, acc, ne, ws, q_ids=w["q"],
+                                q_logits=qpen, stream=stream)
+        st_ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    names = ("projection", "penalize", "pool_policy_accept")
+    st_us = {nm: 1000.0 * statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in st_ev)
+             for j, nm in enumerate(names)}
+    tot = sum(st_us.values())
+    out["penalised_chain_k8"]["stages_us"] = st_us
+    out["penalised_chain_k8"]["stages_pct"] = {nm: 100.0 * v / tot for nm, v in st_us.items()}
 
     # token tree: 3 branches x depth 8 (25 rows)
     parent = torch.from_numpy(synth.tree_parents(3, 8)).to(dev)
@@ -582,6 +606,21 @@ def main():
     proj_ms = [e[0].elapsed_time(e[1]) for e in evs]
     samp_ms = [e[1].elapsed_time(e[2]) for e in evs]
     proj_avg_s = statistics.fmean(proj_ms) / 1000.0
+    # per-window latency of the fused call: events around every window, so
+    # no window overlaps the next (the timed region above lets them overlap
+    # their launch and prologue)
+    n_lat = min(args.steps, 500)
+    lat_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_lat)]
+    torch.cuda.synchronize(dev)
+    for i in range(n_lat):
+        lat_ev[i][0].record(stream)
+        window(i)
+        lat_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    lat_us = sorted(1000.0 * e[0].elapsed_time(e[1]) for e in lat_ev)
+    pct = lambda q: lat_us[min(len(lat_us) - 1, int(q * len(lat_us)))]
+    window_latency = {"p10": pct(0.10), "p50": pct(0.50), "p90": pct(0.90), "windows": n_lat,
+                      "timing": "CUDA events around each fused window"}
     # the pool select alone, on the same logits
     pool_vals = torch.empty((ROWS, 64), dtype=torch.float32, device=dev)
     s0 = torch.cuda.Event(enable_timing=True)
@@ -693,6 +732,11 @@ def main():
                       "pool_policy_accept": 1000.0 * statistics.fmean(samp_ms),
                       "pool_select_only": select_us,
                       "window": 1e6 * job_s / args.steps},
+        "stages_pct_of_window": {
+            "projection": 100.0 * statistics.fmean(proj_ms) / (1000.0 * job_s / args.steps),
+            "pool_policy_accept": 100.0 * statistics.fmean(samp_ms) / (1000.0 * job_s / args.steps),
+            "pool_select_only": 100.0 * select_us / (1e6 * job_s / args.steps)},
+        "window_latency_us": window_latency,
         "rows_sweep_us": sweep,
         "window_cost_model": cost_model,
         "other_workloads": extra,

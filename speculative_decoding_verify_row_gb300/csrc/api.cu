@@ -178,7 +178,7 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
                               any_active && any_q, any_active ? target : nullptr, s);
   int st;
   if (any_active) {
-    st = launch_penalize(tab, rows, target, vocab, any_q, gmax, at<int32_t>(ws, L.status), s);
+    st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);
     if (st != VR_OK) return st;
   }
   return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
@@ -269,7 +269,7 @@ int vr_verify_penalize(float* logits, int rows, int vocab, const int32_t* tokens
   const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_logits, hist,
                                        hist_len, *policy, 0, 0, nullptr, nullptr, nullptr));
   const Layout L = layout(rows, 8, vocab);
-  return launch_penalize(tab, rows, logits, vocab, q_ids != nullptr, nullptr,
+  return launch_penalize(tab, rows, logits, vocab, q_ids != nullptr,
                          at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream));
 }
 

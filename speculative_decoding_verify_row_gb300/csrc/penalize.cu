@@ -7,7 +7,8 @@
 // row(parent[j]), so p and q are penalised by the same H (same section).
 //
 // One CTA per target row and one per draft node: the CTA assembles H in
-// shared memory, each thread takes one history slot, counts that token's
+// shared memory (assemble_history), each thread takes one history slot,
+// counts that token's
 // occurrences and, if the slot is the token's first occurrence, rewrites
 // the logit once.  Distinct tokens never touch the same element, so the
 // scattered writes need no ordering.  Cost: O(W^2) compares per row with
@@ -22,10 +23,11 @@ constexpr int THREADS = 128;
 
 __global__ void __launch_bounds__(THREADS)
     penalize_kernel(const __grid_constant__ ReqTable tab, int rows_total, float* __restrict__ logits, int vocab,
-                    int with_q, uint32_t* __restrict__ gmax, int32_t* status) {
+                    int with_q, int32_t* status) {
   __shared__ int32_t H[VR_MAX_PENALTY_WINDOW];
+  __shared__ int32_t par[VR_MAX_WINDOW_ROWS];
   __shared__ int32_t path[VR_MAX_WINDOW_ROWS];
-  __shared__ int h_len, bad;
+  __shared__ int path_len, bad;
 
   pdl_trigger();
   pdl_wait();
@@ -47,38 +49,11 @@ __global__ void __launch_bounds__(THREADS)
     end_node = rq.parent ? rq.parent[local] : local - 1;
   }
 
-  if (threadIdx.x == 0) {
-    bad = 0;
-    int n = 0, node = end_node, steps = 0;
-    while (node >= 0) {
-      if (node >= rq.n_nodes || steps > rq.n_nodes) {
-        bad = 1;
-        break;
-      }
-      path[n++] = rq.tokens[node];
-      const int p = rq.parent ? rq.parent[node] : node - 1;
-      if (p >= node || p < -1) {
-        bad = 1;
-        break;
-      }
-      node = p;
-      ++steps;
-    }
-    if (bad) {
-      set_status(status, VR_DEV_BAD_PARENT);
-      h_len = 0;
-    } else {
-      // path[] is leaf-first; H = last W of (hist || path root-first)
-      const int W = pol.window;
-      const int from_path = min(n, W);
-      const int from_hist = min(rq.hist_len, W - from_path);
-      h_len = from_hist + from_path;
-      for (int i = 0; i < from_hist; ++i) H[i] = rq.hist[rq.hist_len - from_hist + i];
-      for (int i = 0; i < from_path; ++i) H[from_hist + i] = path[from_path - 1 - i];
-    }
+  int len = assemble_history<THREADS>(rq, end_node, H, par, path, &path_len, &bad);
+  if (len < 0) {
+    if (threadIdx.x == 0) set_status(status, VR_DEV_BAD_PARENT);
+    len = 0;
   }
-  __syncthreads();
-  const int len = h_len;
 
   if (!is_q) {
     float* row = logits + static_cast<size_t>(g) * vocab;
@@ -93,26 +68,6 @@ __global__ void __launch_bounds__(THREADS)
         }
       }
       if (first && t >= 0 && t < vocab) row[t] = penalize_value(__ldcg(row + t), count, pol);
-    }
-    if (gmax) {
-      // refresh the largest order key of every 32-row group a penalty touched
-      __syncthreads();
-      const int ngroups = (vocab + 31) / 32;
-      for (int j = threadIdx.x; j < len; j += THREADS) {
-        const int t = H[j];
-        if (t < 0 || t >= vocab) continue;
-        const int g = t >> 5;
-        bool first = true;
-        for (int i = 0; i < j; ++i)
-          if (H[i] >= 0 && H[i] < vocab && (H[i] >> 5) == g) first = false;
-        if (!first) continue;
-        uint32_t k = 0u;
-        for (int v = g * 32; v < g * 32 + 32 && v < vocab; ++v) {
-          const uint32_t kv = float_key(__ldcg(row + v));
-          k = kv > k ? kv : k;
-        }
-        gmax[static_cast<size_t>(g_row) * ngroups + g] = k;
-      }
     }
   } else {
     // candidates of node `local`, written to the request's q buffer
@@ -135,10 +90,10 @@ __global__ void __launch_bounds__(THREADS)
 // active, and then the q blocks write all 8 candidates (penalised or not),
 // so no separate copy pass is needed.
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab, bool with_q,
-                    uint32_t* gmax, int32_t* status, cudaStream_t stream) {
+                    int32_t* status, cudaStream_t stream) {
   const int blocks = rows_total * (with_q ? 2 : 1);
   return launch_pdl(pen::penalize_kernel, dim3(blocks), dim3(pen::THREADS), 0, stream, tab,
-                    rows_total, logits, vocab, with_q ? 1 : 0, gmax, status) == cudaSuccess
+                    rows_total, logits, vocab, with_q ? 1 : 0, status) == cudaSuccess
              ? VR_OK
              : VR_ERR_CUDA;
 }

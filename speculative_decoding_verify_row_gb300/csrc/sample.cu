@@ -90,6 +90,7 @@ struct RowsShared {
   int ccount;
   // the row's penalty history (built before the wait)
   int32_t H[VR_MAX_PENALTY_WINDOW];
+  int32_t par[VR_MAX_WINDOW_ROWS];
   int32_t path[VR_MAX_WINDOW_ROWS];
   int h_len, h_bad;
 };
@@ -897,37 +898,12 @@ __global__ void __launch_bounds__(THREADS, 2)
 // same arithmetic as the penalty kernel, for the CTA's own row
 
 // H of target row `local`: the last W tokens of (hist || tokens on the path
-// root -> node local - 1).  Thread 0 walks the ancestors, all threads copy.
+// root -> node local - 1), through assemble_history.
 // Sets sr.h_len, and sr.h_bad for a parent array that is not topological.
 __device__ void build_row_history(const ReqDev& rq, int local, RowsShared& sr) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    int n = 0, node = local - 1, steps = 0, bad = 0;
-    while (node >= 0) {
-      if (node >= rq.n_nodes || steps > rq.n_nodes) {
-        bad = 1;
-        break;
-      }
-      sr.path[n++] = rq.tokens[node];
-      const int p = rq.parent ? rq.parent[node] : node - 1;
-      if (p >= node || p < -1) {
-        bad = 1;
-        break;
-      }
-      node = p;
-      ++steps;
-    }
-    sr.h_bad = bad;
-    sr.h_len = n;          // path length for now
-  }
-  __syncthreads();
-  const int n = sr.h_len, W = rq.pol.window;
-  const int from_path = sr.h_bad ? 0 : min(n, W);
-  const int from_hist = sr.h_bad ? 0 : min(rq.hist_len, W - from_path);
-  for (int i = tid; i < from_hist; i += THREADS) sr.H[i] = rq.hist[rq.hist_len - from_hist + i];
-  for (int i = tid; i < from_path; i += THREADS) sr.H[from_hist + i] = sr.path[from_path - 1 - i];
-  __syncthreads();
-  if (tid == 0) sr.h_len = from_hist + from_path;
+  const int len = assemble_history<THREADS>(rq, local - 1, sr.H, sr.par, sr.path, &sr.h_len,
+                                            &sr.h_bad);
+  if (threadIdx.x == 0) sr.h_len = len < 0 ? 0 : len;
   __syncthreads();
 }
 

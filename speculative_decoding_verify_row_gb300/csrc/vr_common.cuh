@@ -164,6 +164,51 @@ __device__ __forceinline__ float vexp(float z) {
 }
 
 // ---------------------------------------------------------------------------
+// penalty history ("Speculative decoding on RDNA" §04): H[0..len) = the last
+// W = pol.window tokens of (hist || tokens on the path root -> end_node),
+// end_node = -1 for the request's root row.  The path follows the parent
+// array (NULL: a chain).  All NT threads of the CTA call it: they stage the
+// parents in shared memory, one thread walks them there, and all copy the
+// history and the path's tokens (the loads overlap).  par and path are
+// shared scratch of VR_MAX_WINDOW_ROWS entries, n_s and bad_s shared ints.
+// Returns len, or -1 (H empty) when the parent array is not topological.
+
+template <int NT>
+__device__ int assemble_history(const ReqDev& rq, int end_node, int32_t* H, int32_t* par,
+                                int32_t* path, int* n_s, int* bad_s) {
+  const int tid = threadIdx.x, nn = rq.n_nodes;
+  for (int j = tid; j < nn; j += NT) par[j] = rq.parent ? rq.parent[j] : j - 1;
+  __syncthreads();
+  if (tid == 0) {
+    int n = 0, node = end_node, bad = 0;
+    while (node >= 0) {
+      if (node >= nn) {
+        bad = 1;
+        break;
+      }
+      path[n++] = node;
+      const int p = par[node];
+      if (p >= node || p < -1) {
+        bad = 1;
+        break;
+      }
+      node = p;
+    }
+    *n_s = n;
+    *bad_s = bad;
+  }
+  __syncthreads();
+  const int bad = *bad_s;
+  const int from_path = bad ? 0 : min(*n_s, rq.pol.window);
+  const int from_hist = bad ? 0 : min(rq.hist_len, rq.pol.window - from_path);
+  for (int i = tid; i < from_hist; i += NT) H[i] = rq.hist[rq.hist_len - from_hist + i];
+  // path[] is leaf-first
+  for (int i = tid; i < from_path; i += NT) H[from_hist + i] = rq.tokens[path[from_path - 1 - i]];
+  __syncthreads();
+  return bad ? -1 : from_hist + from_path;
+}
+
+// ---------------------------------------------------------------------------
 // penalties: one float32 op at a time, round to nearest.
 
 __device__ __forceinline__ float penalize_value(float x, int count, const vr_policy& p) {

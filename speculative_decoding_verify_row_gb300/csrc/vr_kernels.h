@@ -42,9 +42,8 @@ int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int 
                         float* logits, cudaStream_t stream);
 
 // penalties: rows_total rows of `logits` (stride vocab), requests in `tab`
-// gmax (nullable): group maxima of `logits`, refreshed for the touched groups
 int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int vocab,
-                    bool with_q, uint32_t* gmax, int32_t* status, cudaStream_t stream);
+                    bool with_q, int32_t* status, cudaStream_t stream);
 
 // sampling stage, one kernel: logits [rows][vocab] -> pool ids/vals
 // [rows][64]; with a request table also the policy, the per-row decisions
