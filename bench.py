@@ -1,7 +1,7 @@
 """Benchmark of the verify step on one GB300 (or N replicas).
 
-Workload: the sampled chain -- hidden 4096, vocab 151936, k = 3 drafts
-(4 verify rows), bf16 LM-head weights N(0, 0.02), fp32 activations N(0, 1),
+Workload: the sampled chain -- hidden 4096, vocab 151936, three drafts
+and so four rows to verify, bf16 LM-head weights N(0, 0.02), fp32 activations N(0, 1),
 draft q over 8 candidates drawn from the target top-32 with logit = target
 logit + N(0, 1); temperature 0.7, top-k absent (20), min-p 0.05, top-p 0.95,
 no penalties.  One step = one fused verify window (projection, pool,

@@ -89,8 +89,8 @@ extern "C" {
 
 /*
  * Sampler and penalty settings of one request ("Speculative decoding on
- * RDNA" §03: temperature, top-k with absent = 20 and 0 = the 64-wide pool,
- * min-p, top-p; §04: repeat, presence and frequency penalties over the last
+ * RDNA" §03: temperature, top-k (20 when absent, all 64 pool entries when
+ * 0), min-p, top-p; §04: repeat, presence and frequency penalties over the last
  * W tokens).  temperature == 0 means greedy.  Validation (VR_ERR_ARG):
  * temperature, min_p, top_p finite and temperature >= 0; repeat finite and
  * > 0; presence, frequency finite; 0 <= window <= VR_MAX_PENALTY_WINDOW.
@@ -252,9 +252,9 @@ VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, cons
  *     (§02); tree -> the deepest node whose whole path agrees with the
  *     argmax of each parent row (equal depths: the lower node index).
  *   sampled chain: rejection sampling (§03): accept d_i iff
- *     u1 * q_i(d_i) < p_i(d_i) (q_i(d_i) = 0: iff p_i(d_i) > 0); on rejection
- *     emit a draw from (p_i - q_i)+ renormalised (from p_i if that is all
- *     zero) and stop; after k acceptances draw the bonus from p_k.
+ *     u1 * q_i(d_i) < p_i(d_i) (q_i(d_i) = 0: iff p_i(d_i) > 0); a rejected
+ *     d_i is replaced by a sample of (p_i - q_i)+ renormalised (of p_i if
+ *     that is all zero), which ends the window; after k acceptances draw the bonus from p_k.
  *     With q_ids/q_logits (penalised by the caller), q_i is the same policy
  *     on the 8 candidates of node i ordered like the pool.  Without them
  *     (q_ids == NULL: drafts proposed without probabilities, such as n-gram
@@ -372,7 +372,7 @@ VR_API int vr_window_pools(const void* ws, size_t ws_bytes, int rows, int hidden
 
 /*
  * Prompt-lookup draft proposal ("Speculative decoding on RDNA" §06, N-gram
- * takeovers: a request-local n-gram pool over the whole context, default
+ * takeovers: an n-gram index of the request's whole context, by default
  * match 5 / propose 3; "One RDNA4 verify pass has slack for about two dozen
  * speculative tokens", "Spend the budget on a tree": the top few matches
  * become the branches of one token tree).

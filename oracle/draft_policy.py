@@ -1,26 +1,27 @@
 """Oracle (test infrastructure only): the host-side draft proposal and window
 pricing, written plainly from the pages.
 
-  * ngram_propose -- prompt lookup with a request-local n-gram pool
-    ("Speculative decoding on RDNA" §06, N-gram takeovers: match 5, propose
-    3); the top few matches as the branches of one token tree ("One RDNA4
-    verify pass has slack for about two dozen speculative tokens", "Spend
-    the budget on a tree").
+  * ngram_propose -- prompt lookup over an n-gram index of the request's own
+    context ("Speculative decoding on RDNA" §06, N-gram takeovers: match 5,
+    propose 3); several matches become the branches of one token tree ("One
+    RDNA4 verify pass has slack for about two dozen speculative tokens",
+    "Spend the budget on a tree").
     Readings: matches are all earlier occurrences of the last `match`
-    tokens; identical continuations are merged and ranked by how many
-    occurrences propose them (the page's "how often the n-gram recurs"),
-    then by recency (plain prompt lookup takes the most recent match);
-    branches sharing a prefix share its nodes.
+    tokens; identical continuations are merged and ordered by how many
+    occurrences propose them (the page ranks matches by recurrence), then
+    by recency (plain prompt lookup uses the latest occurrence); branches
+    sharing a prefix share its nodes.
   * cost_fit, expected_emitted, choose_depth -- §05 of the first page:
-    window cost = one-row cost + a per-row increment (measured fits), the
-    depth maximising expected emitted tokens (1 plus the running product of
-    per-depth acceptance) per unit of cost, falling back to one token per
-    step when no window beats it.
+    window cost = one-row cost + a per-row increment (measured fits); the
+    chosen depth maximises the expected number of emitted tokens (one, plus
+    the sum over depths of the product of the acceptances up to that depth)
+    divided by the window's cost, and k = 0 (a plain step) is kept unless
+    some window is strictly better.
   * takeover -- §06: an n-gram window takes over when its tokens per unit
     of cost are at least the native window's.
   * ar_floor -- §07: keep speculating only if some probe window is strictly
-    cheaper per emitted token than the timed plain step; a tie or an invalid
-    timing retires.
+    cheaper per emitted token than the timed plain step; equal cost, or a
+    timing that is not a positive finite number, means retiring.
 The CUDA library has its own implementation; nothing here is shared with it.
 """
 import math

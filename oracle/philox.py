@@ -9,8 +9,9 @@ counter words and the round key, the key bumped by Weyl constants between
 rounds), 10 rounds.
 
 Role in the verify step: "Speculative decoding on RDNA" §03 ("how hipfire
-does it") says one request-seeded random stream supplies every draw, so the
-same seed replays the same tokens.  The pages do not name the generator; the
+does it"): all of a request's random draws come from a single stream fixed by
+the request's seed, so replaying a seed reproduces its tokens.  The pages do
+not name the generator; the
 reading taken here is a counter-based Philox, keyed by the request seed and
 addressed by (position, row, purpose), so each draw is a pure function of
 where it is used:

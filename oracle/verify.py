@@ -23,8 +23,8 @@ from .philox import uniform as philox_uniform, PURPOSE_ACCEPT, PURPOSE_EMIT
 from .vexp import vexp, Z_MIN
 
 POOL = 64          # the 64-wide candidate pool ("Speculative decoding on RDNA" §03)
-QCAND = 8          # the draft head's 8 re-scored candidates (same section)
-TOPK_ABSENT = 20   # top-k absent means 20 candidates (same section)
+QCAND = 8          # candidates per draft node, re-scored by the draft head (same section)
+TOPK_ABSENT = 20   # top-k when the request gives none (same section)
 
 
 # ---------------------------------------------------------------------------
@@ -39,7 +39,7 @@ class Policy:
     """Per-request sampler and penalty settings.  Float fields hold float32
     values, as the C struct does."""
     temperature: float = 0.0     # 0 => greedy
-    top_k: int = -1              # <0 absent (=> 20); 0 => whole 64-wide pool
+    top_k: int = -1              # <0 absent (=> 20); 0 => all 64 pool entries
     min_p: float = 0.0           # <=0 disables
     top_p: float = 1.0           # >=1 disables
     repeat: float = 1.0          # 1 disables
@@ -119,9 +119,9 @@ def path_tokens(tokens, parent, node):
 
 
 # ---------------------------------------------------------------------------
-# (a2) penalty histories -- "Speculative decoding on RDNA" §04, figure "the
-# penalty history of verify row i": H_i = last W tokens of (prompt || emitted
-# so far || drafts[0..i)).  For a tree the same rule is read along the node's
+# (a2) penalty histories -- "Speculative decoding on RDNA" §04 and its figure:
+# row i is penalised against H_i, the W most recent tokens of the prompt, the
+# tokens emitted so far and drafts 0..i-1.  For a tree the same rule is read along the node's
 # ancestor path (each branch sees only its own ancestors, as in the masked
 # tree pass of "One RDNA4 verify pass ...").  Fewer than W tokens: use all.
 
@@ -199,8 +199,8 @@ def penalize_candidates(ids, vals, H, pol):
 
 
 # ---------------------------------------------------------------------------
-# (a3) pool -- "Speculative decoding on RDNA" §03: a 64-wide pool with a fixed
-# tie order.  Reading: order by value descending under the total order of
+# (a3) pool -- "Speculative decoding on RDNA" §03: the sampler works on a
+# pool of 64 entries whose ties are broken in one fixed way.  Reading: order by value descending under the total order of
 # float32 that puts every NaN below -inf and -0.0 below +0.0, equal values by
 # ascending token id ("feat(dflash) ...": the top-K selector is held to byte
 # identity with ties, NaN and -inf).  The order is computed on the usual
@@ -244,8 +244,8 @@ def candidate_pool(cand_ids, cand_vals):
 
 # ---------------------------------------------------------------------------
 # (a4) policy -- "Speculative decoding on RDNA" §03 ("how hipfire does it"):
-# temperature, top-k (absent = 20, 0 = the 64-wide pool), min-p and top-p,
-# with the same pool, tie order and summation as the AR sampler.  Reading of
+# temperature, top-k (20 when absent, all 64 pool entries when 0), min-p and
+# top-p, on the AR sampler's pool, tie-breaking and summation.  Reading of
 # the order and arithmetic (the pages fix neither): every step is one
 # float32 operation rounded to nearest, sums run sequentially in pool order,
 #   K = 20 if top_k absent, 64 if 0, else min(top_k, 64); K <= pool size
@@ -389,12 +389,12 @@ def accept_rejection_chain(pdists, qdists, drafts, uniforms, replacement="residu
     steps 1-4; Leviathan et al.; Chen et al.):
       for each draft x = d_i: accept with probability min(1, p_i(x)/q_i(x)),
       tested as u1 * q(x) < p(x) (reading: q(x) = 0 accepts iff p(x) > 0);
-      on rejection emit a draw from (p_i - q_i)+ renormalised (reading: from
-      p_i if that residual is all zero) and end the window;
-      if every draft is accepted, draw the bonus from p_k.
+      a rejected draft is replaced by a sample of (p_i - q_i)+ renormalised
+      (reading: of p_i when that residual is all zero), which ends the window;
+      k accepted drafts are followed by a bonus token sampled from p_k.
     uniforms(row, purpose) gives the window's uniforms.  replacement="p" is
-    the deliberately wrong control of the same section's CPU test (the
-    replacement drawn from p instead of the residual)."""
+    the deliberately wrong control of the same section's CPU test, which
+    samples the replacement from p rather than from the residual)."""
     emitted = []
     for i, x in enumerate(drafts):
         x = int(x)
@@ -430,8 +430,8 @@ def point_mass(token):
     without probabilities (an n-gram match).  Fed to the chain rejection test
     it accepts the token with probability p(token) and, on rejection, draws
     from p with the token removed ("Speculative decoding on RDNA" §06, N-gram
-    takeovers: sampled candidates take the same rejection test with a
-    point-mass draft)."""
+    takeovers: a sampled n-gram candidate is verified by the §03 rejection
+    test with all of q's mass on that candidate)."""
     return RowDist([int(token)], [F32(1.0)], F32(1.0))
 
 
@@ -545,8 +545,9 @@ def verify_window(logits, tokens, parent=None, q_ids=None, q_logits=None, hist=(
 def run_windows(logits_fn, windows, hist, pol, seed, position):
     """Multi-window driver: after each window the emitted ids (never the
     rejected drafts) are appended to the history and the position advances by
-    the number emitted ("Speculative decoding on RDNA" §04 figure note: a
-    rejected draft never enters the next window's history).
+    the number emitted ("Speculative decoding on RDNA" §04 and its figure:
+    the next window's history holds only emitted tokens, never a rejected
+    draft).
     logits_fn(w, hist) -> logits of window w; windows[w] = dict of tokens,
     parent, q_ids, q_logits.  Returns the list of WindowResult and the final
     history."""

@@ -2,8 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
 
-"Speculative decoding on RDNA" §03 ("how hipfire does it") fixes that p is
-the AR sampler's distribution with the same pool, tie order and summation.
+"Speculative decoding on RDNA" §03 ("how hipfire does it") fixes p as the
+AR sampler's distribution, computed on that sampler's pool with its
+tie-breaking and summation.
 For the GPU and this oracle to produce the same kept set and the same draw
 bit for bit, both must evaluate the softmax weights with the same float
 operations, so neither side may call its platform's exp.  The pages fix

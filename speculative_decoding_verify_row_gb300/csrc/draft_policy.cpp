@@ -1,8 +1,8 @@
 // Host-side draft proposal and window-shape policy (no GPU work).
 //
-// (1) Prompt-lookup proposal: a request-local n-gram pool over the whole
-//     context proposes what followed earlier occurrences of the last `match`
-//     tokens ("Speculative decoding on RDNA" §06, N-gram takeovers: default
+// (1) Prompt-lookup proposal: an n-gram index private to the request, over
+//     its whole context, proposes what followed earlier occurrences of the
+//     last `match` tokens ("Speculative decoding on RDNA" §06, N-gram takeovers: default
 //     match 5, propose 3).  Several matches become the branches of one token
 //     tree ("One RDNA4 verify pass has slack for about two dozen speculative
 //     tokens", "Spend the budget on a tree": keep the top few matches, a

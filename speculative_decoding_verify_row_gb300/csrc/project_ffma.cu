@@ -2,8 +2,8 @@
 //
 //   logits[r][v] = sum_h W[v][h] * A[r][h]
 //
-// "Speculative decoding on RDNA" §02: multi-row verify projections must sum
-// in exactly the single-row order.  Here each (r, v) is summed the same way
+// "Speculative decoding on RDNA" §02: a row's sum inside a multi-row verify
+// projection follows the order of the one-row projection.  Here each (r, v) is summed the same way
 // whatever the row count: lane l of a warp owns the 8-wide hidden chunks
 // l, l+32, l+64, ... and accumulates them in that order with one FMA per
 // element (h ascending inside a chunk); the 32 lane sums are then combined

@@ -209,7 +209,7 @@ def test_library_depth_choice_matches_oracle(vb):
 # takeover (§06) and the AR floor (§07)
 
 def test_takeover(vb):
-    # equal pricing takes over ("at least what the native window offers")
+    # equal pricing takes over (the n-gram rate only has to match the native one)
     assert vb.takeover([0.7, 0.7], [0.7, 0.7], 30.0, 7.0) and od.takeover([0.7] * 2, 2, [0.7] * 2, 2, 30.0, 7.0)
     rng = np.random.default_rng(10)
     for trial in range(300):

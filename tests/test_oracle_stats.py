@@ -1,7 +1,8 @@
-"""The CPU statistical test that "Speculative decoding on RDNA" §03 ("lossless,
-precisely") describes: 200,000 sampled windows per case, emitted tokens
-checked against p by a chi-square; drawing the rejection replacement from p
-instead of the residual must fail the same test in every control case."""
+"""The CPU statistical test that "Speculative decoding on RDNA" §03 describes
+for its losslessness claim: 200,000 sampled windows per case, emitted tokens
+checked against p by a chi-square; a control that samples the rejection
+replacement from p, not from the residual, must fail that test in each
+control case."""
 import numpy as np
 import pytest
 from scipy import stats
