@@ -2,8 +2,8 @@
  * verifyrow -- the data-parallel hot path of the speculative-decoding verify
  * step, for one NVIDIA GB300 (sm_103a).
  *
- * One verify window scores the current position plus the draft tokens in a
- * single pass ("Speculative decoding on RDNA", §01 figure "one speculative
+ * One verify window scores the next position and every draft token in one
+ * pass ("Speculative decoding on RDNA", §01 figure "one speculative
  * window": k drafts, k + 1 verify rows), penalises every row against its own
  * history (§04), turns each row into the sampler's distribution (§03 "how
  * hipfire does it") and decides how many drafts to keep (§02 greedy, §03

@@ -436,7 +436,7 @@ def point_mass(token):
 
 
 def accept_naive_descent(pdists, tokens, parent, uniforms):
-    """Naive sampling verify, exact for any deterministic draft ("feat(dflash)
+    """Naive sampling verify, exact when the draft is deterministic ("feat(dflash)
     ...", notes under the spec-step listing): from the root, draw y from the
     current row's p; if a child of the current node carries y (reading: the
     lowest-index such child), move there and repeat; otherwise emit y and

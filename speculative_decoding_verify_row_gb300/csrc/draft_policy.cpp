@@ -5,8 +5,8 @@
 //     last `match` tokens ("Speculative decoding on RDNA" §06, N-gram takeovers: default
 //     match 5, propose 3).  Several matches become the branches of one token
 //     tree ("One RDNA4 verify pass has slack for about two dozen speculative
-//     tokens", "Spend the budget on a tree": keep the top few matches, a
-//     handful of branches at depth six to eight).
+//     tokens", "Spend the budget on a tree": the best few matches, a few
+//     branches six to eight tokens deep).
 // (2) Window pricing: window cost = a + b per extra row, fitted to measured
 //     windows; the draft depth that maximises expected emitted tokens per
 //     unit of cost, with one token per step (no drafts) as the fallback

@@ -1,5 +1,6 @@
 """GPU pool select and sampler policy, bit for bit against the oracle
-("Speculative decoding on RDNA" §03: fixed pool, tie order and summation)."""
+("Speculative decoding on RDNA" §03: the pool, its tie-breaking and the
+summation order are fixed)."""
 import numpy as np
 import pytest
 import torch

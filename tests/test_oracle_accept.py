@@ -313,7 +313,7 @@ def test_point_mass_drafts_are_exact_by_enumeration(V, k, T, seed):
 
 def test_point_mass_chain_has_the_law_of_naive_descent():
     """For a fixed chain the point-mass rejection rule and naive sampling
-    descent (exact for any deterministic draft) emit every sequence with the
+    descent (exact when the draft is deterministic) emit every sequence with the
     same probability, though from different uniforms."""
     rng = np.random.default_rng(43)
     V, k, T = 5, 3, 0.8
