@@ -312,10 +312,10 @@ VR_API int vr_verify_window_batched(const uint16_t* weight, const float* act, in
  * weight, logits and pen_logits are device pointers.  The inputs go into ws:
  * when every input buffer is pinned (page-locked, so mapped into the device's
  * address space) a staging kernel reads them directly, otherwise they are
- * copied.  Then the window runs; a pinned out_ids_h [rows] is written by the
- * kernel, a pageable one copied back; *out_accept_h and *out_n_emitted_h
- * are copied back and the call SYNCHRONISES the stream before returning (one
- * wait per call).
+ * copied.  Then the window runs; pinned output buffers (out_ids_h [rows], and
+ * out_accept_h with out_n_emitted_h) are written by the kernel, pageable ones
+ * copied back; the call SYNCHRONISES the stream before returning (one wait
+ * per call).
  */
 VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
                           int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,

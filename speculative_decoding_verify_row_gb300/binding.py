@@ -11,6 +11,7 @@ stream of the tensors' device unless one is given.
 """
 import ctypes
 import os
+import threading
 from dataclasses import dataclass
 
 import numpy as np
@@ -354,6 +355,19 @@ def _host_ptr(a, dtype, name):
     raise TypeError(f"{name} must be a host torch tensor")
 
 
+_TLS = threading.local()
+
+
+def _pinned_head():
+    """A per-thread pinned int32 pair for accept / n_emitted, so the kernel
+    writes them directly instead of a copy back to pageable memory."""
+    head = getattr(_TLS, "head", None)
+    if head is None:
+        t = torch.zeros(2, dtype=torch.int32).pin_memory()
+        head = _TLS.head = (t, t.numpy())
+    return head
+
+
 def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
                        ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
                        pen_logits=None, path=VR_PATH_AUTO, stream=None):
@@ -366,8 +380,7 @@ def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, 
     _dev(weight, _WEIGHT_DTYPES, "weight")
     _dev(logits, torch.float32, "logits", (R, V))
     _dev(pen_logits, torch.float32, "pen_logits", (R, V))
-    acc = ctypes.c_int32(0)
-    ne = ctypes.c_int32(0)
+    head, head_np = _pinned_head()
     pol = policy.c()
     _check(lib().vr_verify_window_host(_ptr(weight), _host_ptr(act_h, torch.float32, "act_h"), R, H,
                                        V, path, _host_ptr(tokens_h, torch.int32, "tokens_h"),
@@ -378,9 +391,10 @@ def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, 
                                        0 if hist_h is None else hist_h.numel(), ctypes.byref(pol),
                                        seed, position, _ptr(logits), _ptr(pen_logits),
                                        _host_ptr(out_ids_h, torch.int32, "out_ids_h"),
-                                       ctypes.byref(acc), ctypes.byref(ne), _ptr(ws), ws.numel(),
+                                       ctypes.c_void_p(head.data_ptr()),
+                                       ctypes.c_void_p(head.data_ptr() + 4), _ptr(ws), ws.numel(),
                                        _stream(stream, logits.device)), "vr_verify_window_host")
-    return acc.value, ne.value
+    return int(head_np[0]), int(head_np[1])
 
 
 def verify_window_host_async(weight, act_h, tokens_h, policy, seed, position, logits, out_h,

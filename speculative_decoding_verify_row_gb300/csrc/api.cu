@@ -507,22 +507,29 @@ int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, 
   if (st != VR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* out = at<int32_t>(ws, layout(rows, hidden, vocab).st_out);
-  // pinned id buffers are written by the kernel; otherwise staged and copied
+  // pinned output buffers are written by the acceptance kernel; the others
+  // are staged in ws and copied
   int32_t* ids_dev = mapped(out_ids_h);
+  int32_t* acc_dev = mapped(out_accept_h);
+  int32_t* n_dev = mapped(out_n_emitted_h);
+  const bool head_dev = acc_dev && n_dev;
   st = window_host_enqueue(weight, act_h, rows, hidden, vocab, path, tokens_h, parent_h, n_nodes,
                            q_ids_h, q_logits_h, hist_h, hist_len, policy, seed, position, logits,
-                           pen_logits, ws, ws_bytes, s, ids_dev ? ids_dev : out + 2, out, out + 1);
+                           pen_logits, ws, ws_bytes, s, ids_dev ? ids_dev : out + 2,
+                           head_dev ? acc_dev : out, head_dev ? n_dev : out + 1);
   if (st != VR_OK) return st;
-  // accept and n may be pageable, so their copy is the last one enqueued:
-  // the call waits once
+  // a pageable accept/n copy is the last one enqueued: the call waits once
   int32_t head[2];
   if ((!ids_dev && cudaMemcpyAsync(out_ids_h, out + 2, static_cast<size_t>(rows) * sizeof(int32_t),
                                    cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-      cudaMemcpyAsync(head, out, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (!head_dev &&
+       cudaMemcpyAsync(head, out, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return VR_ERR_CUDA;
-  *out_accept_h = head[0];
-  *out_n_emitted_h = head[1];
+  if (!head_dev) {
+    *out_accept_h = head[0];
+    *out_n_emitted_h = head[1];
+  }
   return VR_OK;
 }
 
