@@ -576,3 +576,98 @@ def test_batched_requests_on_crafted_logits(V, path):
         n_em = int(keep[b]["n"].item())
         assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
         assert int(keep[b]["acc"].item()) == ref.accept, b
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH, vb.VR_PATH_FFMA])
+@pytest.mark.parametrize("shape", ["chain", "tree"])
+def test_largest_window_and_penalty_window(shape, path):
+    """The largest window (64 rows: 63 drafts in a chain, or a 63-node tree)
+    with the largest penalty window (W 512 over a 600-token history), sampled,
+    full vocabulary: the result equals the oracle's window on the GPU's own
+    logits, and every pool equals the oracle's pool of the penalised rows."""
+    H, V, R = 64, 151936, vb.VR_MAX_WINDOW_ROWS
+    n = R - 1
+    rng = np.random.default_rng(640 + path)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.3))
+    A = rng.standard_normal((R, H)).astype(np.float32)
+    if shape == "chain":
+        parent = None
+        plist = ov.chain_parents(n)
+    else:
+        # 7 branches of 9 nodes from the root
+        plist = [-1 if j % 9 == 0 else j - 1 for j in range(n)]
+        parent = np.array(plist, np.int32)
+    # drafts: the oracle's argmax of each parent row for most nodes, so the
+    # acceptance walks deep
+    L64 = ov.project(W, A)
+    am = [int(ov.target_pool(L64[r].astype(np.float32))[0][0]) for r in range(R)]
+    tokens = np.array([am[0 if p < 0 else 1 + p] if j % 11 else int(rng.integers(0, V))
+                       for j, p in enumerate(plist)], np.int32)
+    hist = rng.integers(0, V, 600).astype(np.int32)
+    hist[-40:] = tokens[:40] if n >= 40 else hist[-40:]
+    pol = ov.Policy(temperature=0.8, top_k=0, min_p=0.0, top_p=0.97, repeat=1.2, presence=0.5,
+                    frequency=0.1, window=vb.VR_MAX_PENALTY_WINDOW)
+    win = run_window(dev_weight(W), A, tokens, pol, 9, 1000, parent=parent, hist=hist, path=path)
+    g_logits = win["logits"].cpu().numpy()
+    assert_logits_close(g_logits, L64)
+    ref = ov.verify_window(g_logits, tokens, plist, None, None, hist, pol, 9, 1000)
+    pen = win["pen"].cpu().numpy()
+    assert same_bits_f32(pen, ref.pen_logits)
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    vb.window_pools(win["ws"], R, H, V, ids, vals)
+    torch.cuda.synchronize()
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    for r in range(R):
+        want_ids, want_vals = ov.target_pool(pen[r])
+        assert np.array_equal(ids[r], want_ids) and same_bits_f32(vals[r], want_vals), r
+    assert list(win["ids"][:win["n"]]) == ref.emitted and win["accept"] == ref.accept
+    assert win["n"] >= 1
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+def test_largest_batched_call(path):
+    """The largest batched call: VR_MAX_REQUESTS requests of 4 rows each
+    (VR_MAX_ROWS rows in one projection), greedy, sampled and penalised
+    requests mixed; every request equals the oracle's window on the GPU's
+    own logits."""
+    H, V = 64, 5000
+    nreq, k = vb.VR_MAX_REQUESTS, 3
+    R = nreq * (k + 1)
+    assert R == vb.VR_MAX_ROWS
+    rng = np.random.default_rng(1024 + path)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.3))
+    A = rng.standard_normal((R, H)).astype(np.float32)
+    pols = [ov.Policy(), ov.Policy(temperature=0.8, top_k=20, top_p=0.9),
+            ov.Policy(temperature=0.7, top_k=0, min_p=0.05, presence=1.0, window=32),
+            ov.Policy(temperature=0.0, repeat=1.3, window=8)]
+    reqs, keep, specs = [], [], []
+    for b in range(nreq):
+        pol = pols[b % 4]
+        tokens = rng.integers(0, V, k).astype(np.int32)
+        hist = rng.integers(0, V, 50).astype(np.int32)
+        t = dict(tok=dev(tokens), h=dev(hist),
+                 out=torch.full((k + 1,), -7, dtype=torch.int32, device="cuda"),
+                 acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                 n=torch.zeros(1, dtype=torch.int32, device="cuda"))
+        keep.append(t)
+        specs.append((tokens, hist, pol))
+        reqs.append(vb.make_request(k, t["tok"], bpol(pol), b, 77, t["out"], t["acc"], t["n"],
+                                    hist=t["h"]))
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(logits)
+    ws = vb.workspace(R, H, V)
+    vb.verify_window_batched(dev_weight(W), dev(A), reqs, logits, ws, pen_logits=pen, path=path)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    g_logits = logits.cpu().numpy()
+    g_pen = pen.cpu().numpy()
+    assert_logits_close(g_logits[:64], ov.project(W, A[:64]))
+    for b, (tokens, hist, pol) in enumerate(specs):
+        rs = slice(b * (k + 1), (b + 1) * (k + 1))
+        ref = ov.verify_window(g_logits[rs], tokens, None, None, None, hist, pol, b, 77)
+        if ov.penalties_active(pol):
+            assert same_bits_f32(g_pen[rs], ref.pen_logits), b
+        n_em = int(keep[b]["n"].item())
+        assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
+        assert int(keep[b]["acc"].item()) == ref.accept, b
