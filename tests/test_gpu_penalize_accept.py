@@ -162,3 +162,61 @@ def test_point_mass_drafts_match_one_finite_candidate():
         accepted += ref.accept
         rejected += ref.accept < n
     assert accepted > 20 and rejected > 20
+
+
+def special_rows(R, V, rng):
+    """Rows with degenerate values: all NaN, all -inf but one 0, +inf
+    entries, all -inf, a +0/-0 tie on top of negative values, and plain
+    Gaussian rows; NaN with the sign bit set is mixed in."""
+    rows = (rng.standard_normal((R, V)) * 2).astype(np.float32)
+    neg_nan = np.frombuffer(np.uint32(0xFFC00123).tobytes(), np.float32)[0]
+    for r in range(R):
+        kind = r % 6
+        if kind == 0:
+            rows[r] = np.nan
+            rows[r, ::3] = neg_nan
+        elif kind == 1:
+            rows[r] = -np.inf
+            rows[r, 17 % V] = 0.0
+        elif kind == 2:
+            rows[r, 5 % V] = np.inf
+            rows[r, 9 % V] = np.inf
+        elif kind == 3:
+            rows[r] = -np.inf
+        elif kind == 4:
+            rows[r] = -np.abs(rows[r]) - 1.0
+            rows[r, 3 % V] = 0.0
+            rows[r, 30 % V] = -0.0
+    return rows
+
+
+@pytest.mark.parametrize("pi", range(len(ACC_POLICIES)))
+@pytest.mark.parametrize("shape", ["chain_q", "chain_noq", "tree"])
+def test_accept_on_special_values(pi, shape):
+    """Pool, policy and acceptance on rows of NaN, -inf and +inf, on a +0/-0
+    tie and on draft candidates whose logits are -inf: the GPU's decisions
+    equal the oracle's bit for bit."""
+    pol = ACC_POLICIES[pi]
+    rng = np.random.default_rng(77 * pi + len(shape))
+    V = 300
+    for trial in range(12):
+        n = 5 + int(rng.integers(0, 6))
+        pt, parent = random_tree(rng, n, shape != "tree")
+        pen = special_rows(n + 1, V, rng)
+        order = [ov.target_pool(pen[r])[0][:16] for r in range(n + 1)]
+        tokens = np.array([order[ov.row_of(parent[j])][int(rng.integers(0, 4))] for j in range(n)],
+                          np.int32)
+        q_ids = q_log = None
+        if shape == "chain_q":
+            q_ids = np.stack([rng.permutation(order[j])[:8] for j in range(n)]).astype(np.int32)
+            q_ids[:, 0] = tokens
+            q_log = rng.standard_normal((n, 8)).astype(np.float32)
+            q_log[rng.random((n, 8)) < 0.3] = -np.inf
+            q_log[0] = -np.inf
+        seed, position = int(rng.integers(0, 2**63)), int(rng.integers(0, 10**6))
+        ids, acc, ne, st = gpu_accept(pen, tokens, pt, q_ids, q_log, pol, seed, position)
+        ref = ov.verify_window(pen, tokens, parent, q_ids, q_log, (), pol, seed, position)
+        assert st == 0
+        assert (acc, ne) == (ref.accept, ref.n_emitted), (trial, acc, ne, ref.accept)
+        assert list(ids[:ne]) == ref.emitted
+        assert ne >= 1
