@@ -1039,20 +1039,27 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint32_t kv[GPW];
 #pragma unroll
   for (int t = 0; t < GPW; ++t) kv[t] = float_key(fv[t]);
+  // one slot reservation per warp for all of its groups
+  uint64_t cv[GPW];
+  uint32_t ball[GPW];
+  int total = 0;
 #pragma unroll
   for (int t = 0; t < GPW; ++t) {
     const int j = warp + t * (THREADS / 32);
-    if (j >= nchosen) break;
-    const long long v = static_cast<long long>(packed_id(chosen[j])) * 32 + lane;
+    const long long v = static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
     uint64_t c = 0ull;
-    if (v < a.vocab && kv[t] >= tau) c = pack_key_id(kv[t], static_cast<uint32_t>(v));
-    const uint32_t ball = __ballot_sync(0xffffffffu, c != 0ull);
-    if (ball) {
-      int at = 0;
-      if (lane == 0) at = atomicAdd(&sr.ccount, __popc(ball));
-      at = __shfl_sync(0xffffffffu, at, 0);
-      if (c != 0ull) sr.cands[at + __popc(ball & ((1u << lane) - 1u))] = c;
-    }
+    if (j < nchosen && v < a.vocab && kv[t] >= tau) c = pack_key_id(kv[t], static_cast<uint32_t>(v));
+    cv[t] = c;
+    ball[t] = __ballot_sync(0xffffffffu, c != 0ull);
+    total += __popc(ball[t]);
+  }
+  int at = 0;
+  if (lane == 0 && total) at = atomicAdd(&sr.ccount, total);
+  at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+  for (int t = 0; t < GPW; ++t) {
+    if (cv[t] != 0ull) sr.cands[at + __popc(ball[t] & ((1u << lane) - 1u))] = cv[t];
+    at += __popc(ball[t]);
   }
   __syncthreads();
 
