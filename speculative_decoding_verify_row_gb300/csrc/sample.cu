@@ -931,21 +931,39 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
   __threadfence();     // the rewritten logits reach L2 before anyone reads them there
   __syncthreads();
   // a warp per history slot: the first slot of each touched group refreshes
-  // that group's maximum from the penalised row
-  for (int j = warp; j < len; j += THREADS / 32) {
-    const int t = sr.H[j];
-    if (t < 0 || t >= vocab) continue;
-    const int g = t >> 5;
-    bool seen = false;
-    for (int i = lane; i < j; i += 32) {
-      const int u = sr.H[i];
-      seen |= (u >= 0) & (u < vocab) & ((u >> 5) == g);
+  // that group's maximum from the penalised row.  A warp takes eight of its
+  // slots at a time and issues their loads together.
+  constexpr int NW = THREADS / 32, SB = 8;
+  for (int j0 = warp; j0 < len; j0 += NW * SB) {
+    int gs[SB];
+    float x[SB];
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      const int j = j0 + b * NW;       // the same for every lane of the warp
+      int g = -1;
+      if (j < len) {
+        const int t = sr.H[j];
+        if (t >= 0 && t < vocab) {
+          g = t >> 5;
+          bool seen = false;
+          for (int i = lane; i < j; i += 32) {
+            const int u = sr.H[i];
+            seen |= (u >= 0) & (u < vocab) & ((u >> 5) == g);
+          }
+          if (__any_sync(0xffffffffu, seen)) g = -1;
+        }
+      }
+      gs[b] = g;
+      const long long v = static_cast<long long>(g < 0 ? 0 : g) * 32 + lane;
+      x[b] = __ldcg(row + (v < vocab ? v : 0));     // unconditional: loads overlap
     }
-    if (__any_sync(0xffffffffu, seen)) continue;
-    const int v = g * 32 + lane;
-    const uint32_t k = v < vocab ? float_key(__ldcg(row + v)) : 0u;
-    const uint32_t m = __reduce_max_sync(0xffffffffu, k);
-    if (lane == 0) gmax_row[g] = m;
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      if (gs[b] < 0) continue;
+      const int v = gs[b] * 32 + lane;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, v < vocab ? float_key(x[b]) : 0u);
+      if (lane == 0) gmax_row[gs[b]] = m;
+    }
   }
   // the node's draft candidates, penalised with this row's history
   const bool chain_node = rq.q_ids && local < rq.n_nodes &&
