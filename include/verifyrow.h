@@ -358,7 +358,9 @@ VR_API int vr_verify_window_host_async(const uint16_t* weight, const float* act_
  * pointers, caller-owned).  Each row is the top 64 of that row's logits
  * after its penalties, in pool order ("Speculative decoding on RDNA" §03:
  * value descending, token id ascending, NaN lowest); entries past the
- * vocabulary are id -1.  rows, hidden and vocab are those of that call
+ * vocabulary are id -1.  For the rows of a greedy request (temperature 0)
+ * only entry 0, the argmax, is defined, since that is all a greedy decision
+ * uses; the other entries may be id -1.  rows, hidden and vocab are those of that call
  * (the batched call: its total rows).  Argument errors return before
  * anything is enqueued.
  */

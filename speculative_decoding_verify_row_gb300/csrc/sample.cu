@@ -789,10 +789,11 @@ __device__ __forceinline__ void sort_out_into_sorted(SelectShared& sh) {
 // values, then the row's decisions, then (last row of its request) the
 // acceptance walk.
 __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, const uint64_t* pool,
-                           RowShared& rs, AcceptShared& as, int& last, bool prepared) {
+                           RowShared& rs, AcceptShared& as, int& last, bool prepared,
+                           int n_pool = kPool) {
   const int tid = threadIdx.x;
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
-  const int n = a.vocab < kPool ? a.vocab : kPool;
+  const int n = min(a.vocab, n_pool);
   if (tid < kPool) {
     int32_t id = -1;
     float v = __int_as_float(0x7fffffff);
@@ -1014,6 +1015,45 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (sr.h_bad && tid == 0) set_status(a.status, VR_DEV_BAD_PARENT);
     penalize_own_row(rq0, row - rq0.row0, a.pen_logits + static_cast<size_t>(row) * a.vocab,
                      a.vocab, gmax + static_cast<size_t>(row) * ngroups, sr);
+  }
+
+  if (rq0.pol.temperature == 0.f) {
+    // a greedy request needs only each row's argmax: the largest key among
+    // the group maxima, the lowest group holding it, and the lowest id of
+    // that key inside the group (the pool's first entry; no other entry is
+    // formed)
+    uint64_t best = 0ull;
+#pragma unroll
+    for (int i = 0; i < GI_MAX; ++i) {
+      const int g = i * THREADS + tid;
+      const uint32_t k = __ldcg(gm + (g < ngroups ? g : 0));   // unconditional: loads overlap
+      const uint64_t c = g < ngroups ? pack_key_id(k, static_cast<uint32_t>(g)) : 0ull;
+      best = c > best ? c : best;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    if (lane == 0) sr.pool[1 + warp] = best;
+    __syncthreads();
+    if (warp == 0) {
+      uint64_t b = lane < THREADS / 32 ? sr.pool[1 + lane] : 0ull;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, b, o);
+        b = other > b ? other : b;
+      }
+      const uint32_t key = static_cast<uint32_t>(b >> 32);
+      const long long v = static_cast<long long>(packed_id(b)) * 32 + lane;
+      const uint32_t kv = float_key(__ldcg(rp + (v < a.vocab ? v : 0)));
+      const uint32_t ball = __ballot_sync(0xffffffffu, v < a.vocab && kv == key);
+      const long long id = v - lane + (ball ? __ffs(ball) - 1 : 0);
+      if (lane == 0) sr.pool[0] = pack_key_id(key, static_cast<uint32_t>(id));
+    }
+    __syncthreads();
+    finish_row(a, tab, row, sr.pool, rs, as, last, true, 1);
+    return;
   }
 
   // (a) top 64 groups, as composites (max key << 32) | ~group
