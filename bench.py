@@ -48,7 +48,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the penalised-chain, tree and batched workloads")
-    p.add_argument("--mode", choices=["full", "window", "project", "project_batched", "topk"],
+    p.add_argument("--mode", choices=["full", "window", "project", "project_batched", "batched",
+                                      "topk"],
                    default="full",
                    help="window: only the timed windows (for a profiler's launch list); "
                         "project: only the projection of one window (for a kernel capture); "
@@ -235,6 +236,38 @@ def _event_time(torch, stream, fn, n):
     return t0.elapsed_time(t1) / 1000.0 / n
 
 
+def batched_serving(torch, vb, synth, dev):
+    """The batched-serving workload: 64 requests x k 3 (256 rows) at hidden
+    5120; even requests greedy, odd ones T 0.8 / top-k 20 / top-p 0.9 /
+    presence 1.5 over 2048-token Zipf histories (W 64)."""
+    H5, nreq, k = 5120, 64, 3
+    W5 = synth.weights(V, H5)
+    wd5 = torch.from_numpy(W5.view(np.int16)).to(dev)
+    del W5
+    R = nreq * (k + 1)
+    A = torch.from_numpy(synth.activations(R, H5, 500)).to(dev)
+    rng = np.random.default_rng(500)
+    keep, reqs = [], []
+    for b in range(nreq):
+        greedy = b % 2 == 0
+        bpol = vb.Policy() if greedy else vb.Policy(temperature=0.8, top_k=20, top_p=0.9,
+                                                     presence=1.5, window=64)
+        qi = rng.integers(0, V, (k, 8)).astype(np.int32)
+        ql = rng.standard_normal((k, 8)).astype(np.float32)
+        t = dict(d=torch.from_numpy(qi[:, 0].copy()).to(dev), q=torch.from_numpy(qi).to(dev),
+                 ql=torch.from_numpy(ql).to(dev),
+                 h=torch.from_numpy(synth.zipf_history(2048, V, seed=1000 + b)).to(dev),
+                 o=torch.empty(k + 1, dtype=torch.int32, device=dev),
+                 a=torch.empty(1, dtype=torch.int32, device=dev),
+                 n=torch.empty(1, dtype=torch.int32, device=dev))
+        keep.append(t)
+        reqs.append(vb.make_request(k, t["d"], bpol, b, 2048, t["o"], t["a"], t["n"], q_ids=t["q"],
+                                    q_logits=t["ql"], hist=t["h"]))
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    return dict(H5=H5, nreq=nreq, R=R, wd5=wd5, A=A, reqs=reqs, keep=keep, lg=lg,
+                pen=torch.empty_like(lg), ws=vb.workspace(R, H5, V, device=dev))
+
+
 def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
     """The other verify workloads on the same GPU: the penalised chain (k 8),
     the 3 x 8 token tree (greedy and sampled) and 64 batched requests at
@@ -326,32 +359,9 @@ def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
     del wins, twins, lg, pen, ws
 
     # batched serving: 64 requests x k 3 at hidden 5120
-    H5, nreq, k = 5120, 64, 3
-    W5 = synth.weights(V, H5)
-    wd5 = torch.from_numpy(W5.view(np.int16)).to(dev)
-    del W5
-    R = nreq * (k + 1)
-    A = torch.from_numpy(synth.activations(R, H5, 500)).to(dev)
-    rng = np.random.default_rng(500)
-    keep, reqs = [], []
-    for b in range(nreq):
-        greedy = b % 2 == 0
-        bpol = vb.Policy() if greedy else vb.Policy(temperature=0.8, top_k=20, top_p=0.9,
-                                                     presence=1.5, window=64)
-        qi = rng.integers(0, V, (k, 8)).astype(np.int32)
-        ql = rng.standard_normal((k, 8)).astype(np.float32)
-        t = dict(d=torch.from_numpy(qi[:, 0].copy()).to(dev), q=torch.from_numpy(qi).to(dev),
-                 ql=torch.from_numpy(ql).to(dev),
-                 h=torch.from_numpy(synth.zipf_history(2048, V, seed=1000 + b)).to(dev),
-                 o=torch.empty(k + 1, dtype=torch.int32, device=dev),
-                 a=torch.empty(1, dtype=torch.int32, device=dev),
-                 n=torch.empty(1, dtype=torch.int32, device=dev))
-        keep.append(t)
-        reqs.append(vb.make_request(k, t["d"], bpol, b, 2048, t["o"], t["a"], t["n"], q_ids=t["q"],
-                                    q_logits=t["ql"], hist=t["h"]))
-    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
-    pen = torch.empty_like(lg)
-    ws = vb.workspace(R, H5, V, device=dev)
+    bs = batched_serving(torch, vb, synth, dev)
+    wd5, A, reqs, lg, pen, ws = bs["wd5"], bs["A"], bs["reqs"], bs["lg"], bs["pen"], bs["ws"]
+    H5, nreq, R = bs["H5"], bs["nreq"], bs["R"]
 
     def batched(i):
         vb.verify_window_batched(wd5, A, reqs, lg, ws, pen_logits=pen, path=vb.VR_PATH_TC_BATCH,
@@ -497,6 +507,30 @@ def run_projection_only(torch, vb, synth, wd, dev, args):
                       "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
 
 
+def run_batched_only(torch, vb, synth, dev, args):
+    """The batched-serving call (64 requests x 4 rows, hidden 5120, batch
+    tensor-core path): warm-up, then steps timed with events."""
+    bs = batched_serving(torch, vb, synth, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(i):
+        vb.verify_window_batched(bs["wd5"], bs["A"], bs["reqs"], bs["lg"], bs["ws"],
+                                 pen_logits=bs["pen"], path=vb.VR_PATH_TC_BATCH, stream=stream)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = 1000.0 * e0.elapsed_time(e1) / max(1, args.steps)
+    print(json.dumps({"mode": "batched", "steps": args.steps, "us_per_call": us,
+                      "request_windows_per_s": bs["nreq"] / us * 1e6}))
+
+
 def run_batched_projection_only(torch, vb, synth, dev, args):
     """The batched-serving projection (256 rows, hidden 5120, tensor-core batch
     path), warm-up + steps times."""
@@ -536,6 +570,9 @@ def main():
         return
     if args.mode == "project_batched":
         run_batched_projection_only(torch, vb, synth, dev, args)
+        return
+    if args.mode == "batched":
+        run_batched_only(torch, vb, synth, dev, args)
         return
     W = synth.weights(V, H)
     wd = torch.from_numpy(W.view(np.int16)).to(dev)
