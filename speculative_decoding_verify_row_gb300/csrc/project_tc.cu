@@ -575,7 +575,15 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
   if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::MT * tc::BM)) return VR_ERR_ARG;
   const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
   const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
-  const int grid = std::min(n_units, g_num_sms);
+  // One CTA per SM; or, when fewer CTAs take the same number of units each
+  // and the SMs this leaves free can hold the row sampling kernel that
+  // follows in a window (one CTA per row, two per SM), that smaller grid:
+  // the sampling kernel then sits beside the projection, and the next
+  // window's projection CTAs all start on SMs of their own.
+  int grid = std::min(n_units, g_num_sms);
+  const int per_cta = (n_units + g_num_sms - 1) / g_num_sms;
+  const int balanced = (n_units + per_cta - 1) / per_cta;
+  if ((rows + 1) / 2 <= g_num_sms - balanced) grid = balanced;
 
   if (rows <= tc::FUSED_MAX_ROWS) {
     // one group, planes built in the kernel from the activations
