@@ -20,6 +20,9 @@ def env_world():
 def init(backend):
     rank, world, local = env_world()
     if world > 1 and not dist.is_initialized():
+        if backend == "nccl":
+            # each rank's own GPU before NCCL binds its communicator
+            torch.cuda.set_device(local)
         dist.init_process_group(backend=backend, rank=rank, world_size=world)
     return rank, world, local
 
