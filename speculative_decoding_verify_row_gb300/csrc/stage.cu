@@ -28,6 +28,12 @@ __device__ __forceinline__ int seg_of(const StageArgs& a, uint32_t w) {
 
 __global__ void __launch_bounds__(kStageThreads)
     stage_inputs_kernel(const __grid_constant__ StageArgs a) {
+  // The kernel that follows (a projection or its split pass) reads nothing
+  // of the window before its own wait, only the weights, so it may launch
+  // at once and start its weight stream while the previous window ends.
+  // The kernels after it launch only once it is past its wait, by which
+  // time this kernel has completed.
+  pdl_trigger();
   const uint32_t total = a.end[a.nseg - 1];
   const uint32_t base = blockIdx.x * (kStageThreads * kStagePerThread) + threadIdx.x;
   uint32_t v[kStagePerThread];
@@ -44,8 +50,6 @@ __global__ void __launch_bounds__(kStageThreads)
   }
   // the workspace may still be read by the previous window's kernels
   pdl_wait();
-  // this kernel starts a window: dependents launch once it is past its wait
-  pdl_trigger();
 #pragma unroll
   for (int i = 0; i < kStagePerThread; ++i) {
     const uint32_t w = base + i * kStageThreads;
