@@ -145,11 +145,11 @@ __device__ __forceinline__ void split_block(uint8_t* btile, int rows_in_group, i
 // rows past R zero; the same hi/mid/lo split.
 __global__ void split_planes_kernel(const float* __restrict__ act, int rows, int hidden,
                                     int groups, __nv_bfloat16* __restrict__ planes) {
-  pdl_wait();
-  // a window starts with this kernel: its dependents may launch only now,
-  // once every kernel before the window is complete, because the later
-  // kernels of the window read the window's inputs before their own wait
+  // the projection that follows reads only the weights before its own
+  // wait, so it may launch at once and start its weight stream; the kernels
+  // after it launch only once it is past its wait
   pdl_trigger();
+  pdl_wait();
   const int chunks = hidden / 8;
   const long long total = static_cast<long long>(groups) * NP * chunks;
   const float2 neg1 = make_float2(-1.0f, -1.0f);

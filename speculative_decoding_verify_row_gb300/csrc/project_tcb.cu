@@ -303,11 +303,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 // (the subtraction is exact); rows past R are zero.
 __global__ void split_planes2_kernel(const float* __restrict__ act, int rows, int hidden,
                                      int groups, __nv_bfloat16* __restrict__ planes) {
-  pdl_wait();
-  // a window starts with this kernel: its dependents may launch only now,
-  // once every kernel before the window is complete, because the later
-  // kernels of the window read the window's inputs before their own wait
+  // the projection that follows reads only the weights before its own
+  // wait, so it may launch at once and start its weight stream; the kernels
+  // after it launch only once it is past its wait
   pdl_trigger();
+  pdl_wait();
   const int chunks = hidden / 8;
   const long long total = static_cast<long long>(groups) * GROUP * chunks;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;

@@ -351,13 +351,13 @@ __device__ __forceinline__ void policy_warp(const float* vals, int n, const vr_p
 // predecessor grid to complete (wait) before it touches any buffer that a
 // predecessor may write or read, and lets the next kernel on the stream
 // start launching early (launch_dependents): at once, except the
-// projections and their split passes, which trigger only after their own
-// wait.  So every kernel after a window's projection starts after
-// everything before the window is complete and may read the window's
-// inputs (drafts, candidates, parents) before its own wait, as the row
-// sampling kernel does.  Before their wait the projections touch only the
-// weights, which no kernel of a window writes; so the host-input staging
-// kernel, which precedes them, triggers at once.  Completion still follows
+// projections, which trigger only after their own wait.  So every kernel
+// after a window's projection starts after everything before the window is
+// complete and may read the window's inputs (drafts, candidates, parents)
+// before its own wait, as the row sampling kernel does.  Before their wait
+// the projections touch only the weights, which no kernel of a window
+// writes; so the kernels that precede them in a window (the host-input
+// staging kernel, the split passes) trigger at once.  Completion still follows
 // stream order; only launch latency, prologues and the first weight loads
 // overlap.  Without the launch attribute both are no-ops.
 
