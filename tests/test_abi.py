@@ -80,3 +80,24 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
         assert lib.vr_topk(p, 15, 248320, k, p, p, p, 1 << 30, None) == -1
     assert lib.vr_topk(p, 15, 248320, 16, None, p, p, 1 << 30, None) == -1
     assert lib.vr_topk(p, 15, 248320, 16, p, p, p, 64, None) == -5
+
+
+def test_host_window_and_pool_arguments_are_rejected_on_the_host(lib):
+    from speculative_decoding_verify_row_gb300.binding import vr_policy
+    p = ctypes.c_void_p(256)            # never dereferenced: validation fails first
+    good = vr_policy(0.7, -1, 0.0, 1.0, 1.0, 0.0, 0.0, 0)
+    bad = vr_policy(-1.0, -1, 0.0, 1.0, 1.0, 0.0, 0.0, 0)
+
+    def host_async(rows, nodes, pol, out_h, ws_bytes):
+        return lib.vr_verify_window_host_async(p, p, rows, 4096, 100, 0, p, None, nodes, None, None,
+                                               None, 0, ctypes.byref(pol), 0, 0, p, None, out_h, p,
+                                               ws_bytes, None)
+    assert host_async(4, 3, good, None, 1 << 30) == -1          # no result buffer
+    assert host_async(4, 3, bad, p, 1 << 30) == -1              # negative temperature
+    assert host_async(4, 2, good, p, 1 << 30) == -1             # rows != nodes + 1
+    assert host_async(4, 3, good, p, 16) == -5                  # workspace too small
+    # pools of the last window: outputs, shape and workspace are checked
+    assert lib.vr_window_pools(p, 1 << 30, 4, 4096, 100, None, p, None) == -1
+    assert lib.vr_window_pools(p, 1 << 30, 0, 4096, 100, p, p, None) == -1
+    assert lib.vr_window_pools(p, 16, 4, 4096, 100, p, p, None) == -5
+    assert lib.vr_window_pools(None, 1 << 30, 4, 4096, 100, p, p, None) == -5
