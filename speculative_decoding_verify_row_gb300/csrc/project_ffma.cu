@@ -179,10 +179,8 @@ int launch_project_ffma(const uint16_t* weight, const float* act, int rows, int 
                         float* logits, cudaStream_t stream) {
   const int rb_max = ffma_rows_per_pass(hidden);
   if (rb_max < 1) return VR_ERR_UNSUPPORTED;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return VR_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return VR_ERR_CUDA;
   for (int r0 = 0; r0 < rows; r0 += rb_max) {
     const int rb = std::min(rb_max, rows - r0);
     int st;

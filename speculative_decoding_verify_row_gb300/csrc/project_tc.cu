@@ -471,28 +471,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 // host side
 
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-bool get_encoder() {
-  if (g_encode) return true;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || !fn)
-    return false;
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  return true;
+// The driver's tensor-map encoder, looked up once per process (a driver entry
+// point, the same for every device); null if the driver lacks it.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
 }
-
-int g_num_sms = 0;
 }  // namespace
 
 // 2-D bf16 tensor map over a row-major [outer][inner] array, tiles of
 // box_outer x box_inner elements, 128-byte swizzle (box_inner * 2 == 128).
 bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                       uint32_t box_inner, uint32_t box_outer) {
-  if (!get_encoder()) return false;
+  const auto g_encode = encoder();
+  if (!g_encode) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -508,7 +508,8 @@ bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64
 // parts of a box past the array are not written.
 bool encode_f32_box_sw128(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer) {
-  if (!get_encoder()) return false;
+  const auto g_encode = encoder();
+  if (!g_encode) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 4};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -523,7 +524,8 @@ bool encode_f32_box_sw128(CUtensorMap* map, const void* base, uint64_t inner, ui
 // box_outer x box_inner elements, no swizzle; reads past the array are zero.
 bool encode_f32_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint32_t box_inner, uint32_t box_outer) {
-  if (!get_encoder()) return false;
+  const auto g_encode = encoder();
+  if (!g_encode) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 4};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -540,13 +542,9 @@ template <int NIT>
 cudaError_t launch_group(const CUtensorMap& tm_w, const CUtensorMap& tm_x, int hidden, int vocab,
                          int rg, int row_base, float* logits, float* logits2, uint32_t* gmax,
                          int32_t* status, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        tc::project_tc_kernel<NIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  const cudaError_t e = set_smem_limit_once(tc::project_tc_kernel<NIT>, tc::SMEM_BYTES, attr_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(tc::project_tc_kernel<NIT>, dim3(grid), dim3(tc::THREADS), tc::SMEM_BYTES,
                     stream, tm_w, tm_x, hidden, vocab, rg, row_base, logits, logits2, gmax,
                     (vocab + 31) / 32, status);
@@ -564,12 +562,8 @@ size_t tc_scratch_bytes(int rows, int hidden) {
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, float* logits2, void* scratch, uint32_t* gmax,
                       int32_t* status, cudaStream_t stream) {
-  if (!g_num_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return VR_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return VR_ERR_CUDA;
-  }
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return VR_ERR_CUDA;
   CUtensorMap tm_w;
   // one 256-row box per unit and K block (both vocab tiles of the unit)
   if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::MT * tc::BM)) return VR_ERR_ARG;
@@ -580,10 +574,10 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
   // follows in a window (one CTA per row, two per SM), that smaller grid:
   // the sampling kernel then sits beside the projection, and the next
   // window's projection CTAs all start on SMs of their own.
-  int grid = std::min(n_units, g_num_sms);
-  const int per_cta = (n_units + g_num_sms - 1) / g_num_sms;
+  int grid = std::min(n_units, num_sms);
+  const int per_cta = (n_units + num_sms - 1) / num_sms;
   const int balanced = (n_units + per_cta - 1) / per_cta;
-  if ((rows + 1) / 2 <= g_num_sms - balanced) grid = balanced;
+  if ((rows + 1) / 2 <= num_sms - balanced) grid = balanced;
 
   if (rows <= tc::FUSED_MAX_ROWS) {
     // one group, planes built in the kernel from the activations
@@ -619,7 +613,7 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
     const long long work = static_cast<long long>(groups) * tc::NP * (hidden / 8);
     const int threads = 256;
     const int blocks = static_cast<int>(std::min<long long>((work + threads - 1) / threads,
-                                                            static_cast<long long>(g_num_sms) * 8));
+                                                            static_cast<long long>(num_sms) * 8));
     if (launch_pdl(tc::split_planes_kernel, dim3(blocks), dim3(threads), 0, stream, act, rows,
                    hidden, groups, pl) != cudaSuccess)
       return VR_ERR_CUDA;

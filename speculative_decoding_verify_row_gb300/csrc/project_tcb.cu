@@ -333,8 +333,6 @@ __global__ void split_planes2_kernel(const float* __restrict__ act, int rows, in
 }  // namespace tcb
 
 namespace {
-int g_tcb_sms = 0;
-bool g_tcb_attr = false;
 }  // namespace
 
 size_t tcb_plane_bytes(int rows, int hidden) {
@@ -345,25 +343,18 @@ size_t tcb_plane_bytes(int rows, int hidden) {
 int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                        float* logits, float* logits2, void* planes, uint32_t* gmax,
                        int32_t* status, cudaStream_t stream) {
-  if (!g_tcb_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_tcb_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return VR_ERR_CUDA;
-  }
-  if (!g_tcb_attr) {
-    if (cudaFuncSetAttribute(tcb::project_tcb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tcb::SMEM_BYTES) != cudaSuccess)
-      return VR_ERR_CUDA;
-    g_tcb_attr = true;
-  }
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return VR_ERR_CUDA;
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (set_smem_limit_once(tcb::project_tcb_kernel, tcb::SMEM_BYTES, attr_set) != cudaSuccess)
+    return VR_ERR_CUDA;
   const int groups = (rows + tcb::GROUP - 1) / tcb::GROUP;
   auto* pl = static_cast<__nv_bfloat16*>(planes);
   {
     const long long work = static_cast<long long>(groups) * tcb::GROUP * (hidden / 8);
     const int threads = 256;
     const int blocks = static_cast<int>(std::min<long long>((work + threads - 1) / threads,
-                                                            static_cast<long long>(g_tcb_sms) * 8));
+                                                            static_cast<long long>(num_sms) * 8));
     if (launch_pdl(tcb::split_planes2_kernel, dim3(blocks), dim3(threads), 0, stream, act, rows,
                    hidden, groups, pl) != cudaSuccess)
       return VR_ERR_CUDA;
@@ -371,7 +362,7 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
   CUtensorMap tm_w;
   if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tcb::BK, tcb::BN)) return VR_ERR_ARG;
   const int n_tiles = (vocab + tcb::BN - 1) / tcb::BN;
-  const int grid = std::min(n_tiles, g_tcb_sms);
+  const int grid = std::min(n_tiles, num_sms);
   const int vec_ok = (vocab % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(logits2) % 16 == 0);
   // the staged epilogue's tensor stores: fp32 boxes of 32 columns x 128 rows

@@ -1212,13 +1212,9 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.q_after_wait = 1;
   a.pen_logits = nullptr;
   const size_t smem = sizeof(smp::StageShared);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(smp::sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return VR_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (set_smem_limit_once(smp::sample_kernel, static_cast<int>(smem), attr_set) != cudaSuccess)
+    return VR_ERR_CUDA;
   ReqTable none{};
   return launch_pdl(smp::sample_kernel, dim3(nseg, rows), dim3(smp::THREADS), smem, stream, a,
                     tab ? *tab : none) == cudaSuccess
@@ -1247,13 +1243,9 @@ int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
   a.q_after_wait = q_after_wait ? 1 : 0;
   a.pen_logits = pen_logits;
   const size_t smem = sizeof(smp::RowsShared);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(smp::sample_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return VR_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (set_smem_limit_once(smp::sample_rows_kernel, static_cast<int>(smem), attr_set) != cudaSuccess)
+    return VR_ERR_CUDA;
   return launch_pdl(smp::sample_rows_kernel, dim3(rows), dim3(smp::THREADS), smem, stream, a, tab,
                     gmax, (vocab + 31) / 32) == cudaSuccess
              ? VR_OK

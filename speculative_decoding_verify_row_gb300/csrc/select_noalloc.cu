@@ -39,7 +39,6 @@ constexpr size_t kCounterSlots = 32;   // 256 bytes holding the 32 uint32 row co
 // 1 MiB + 256 B
 static __device__ __align__(256) uint64_t g_select_scratch[kCounterSlots + kNoallocSlots];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 uint64_t* g_scratch_ptr[kMaxDevices] = {};
 

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -9,6 +10,43 @@
 #include "vr_common.cuh"
 
 namespace vr {
+
+// Per-device host state.  A kernel's dynamic shared-memory limit and the SM
+// count belong to a device, not to the process, so the launchers remember
+// them per device ordinal.  Two threads may both fill one entry; they store
+// the same value.
+constexpr int kMaxDevices = 64;
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) on the
+// current device, once per device; `done` is the kernel's own flag array.
+// Devices past kMaxDevices get the call on every launch.
+template <class K>
+inline cudaError_t set_smem_limit_once(K kernel, int bytes,
+                                       std::atomic<bool> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// SM count of the current device (looked up once per device); 0 on failure.
+inline int device_sm_count() {
+  static std::atomic<int> sms[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int n = sms[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) sms[dev].store(n, std::memory_order_release);
+  return n;
+}
 
 // host inputs -> workspace by a kernel that reads device-mapped pinned host
 // memory (src: device addresses of pinned host buffers; dst: workspace)
