@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
+  __syncwarp();     // lanes of warps 0 and 1 took single-lane branches above
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
@@ -289,6 +290,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   // the tensor stores issued by the epilogue have written their data
   if (staged && threadIdx.x == 64) bulk_wait_all();
   tc_fence_before();
+  // Each role above runs on one lane of its warp (producer, MMA issuer) while
+  // the other lanes come straight here, so a warp's lanes reach this point at
+  // different times.  The block barrier counts arrivals per warp, so a warp
+  // must arrive as a whole: without the reconvergence below, the same barrier
+  // of the chain projection kernel was measured to release while its
+  // epilogue warps were still reading TMEM, and the dealloc that follows it
+  // could then free TMEM in use.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();

@@ -132,7 +132,7 @@ __device__ __forceinline__ void find_digit(int nb, int need, SelectShared& sh) {
   for (int c = 0; c < per_warp; c += 32) total += sh.hist[top - 1 - c - lane];
   total = __reduce_add_sync(0xffffffffu, total);
   if (lane == 0) sh.warp_sum[warp] = total;
-  __syncthreads();
+  block_sync();
   uint32_t cum = 0;
   for (int w = 0; w < warp; ++w) cum += sh.warp_sum[w];
   if (cum < static_cast<uint32_t>(need) && cum + total >= static_cast<uint32_t>(need)) {
@@ -153,7 +153,7 @@ __device__ __forceinline__ void find_digit(int nb, int need, SelectShared& sh) {
       cum += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  __syncthreads();
+  block_sync();
 }
 
 // Top-64 of the nonzero composites held by the block (ITEMS per thread),
@@ -173,10 +173,10 @@ __device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
     sh.count = 0;
     sh.gcount = 0;
   }
-  __syncthreads();
+  block_sync();
   mine = __reduce_add_sync(0xffffffffu, mine);
   if (lane == 0) atomicAdd(&sh.n_valid, mine);
-  __syncthreads();
+  block_sync();
 
   uint64_t prefix = 0ull, mask = 0ull;
   bool gathered = false;
@@ -188,25 +188,25 @@ __device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
       const int nb = 1 << bits;
       shift -= bits;
       for (int b = tid; b < nb; b += THREADS) sh.hist[b] = 0u;
-      __syncthreads();
+      block_sync();
 #pragma unroll
       for (int i = 0; i < N; ++i)
         if (x[i] != 0ull && (x[i] & mask) == prefix)
           atomicAdd(&sh.hist[static_cast<uint32_t>(x[i] >> shift) & (nb - 1)], 1u);
-      __syncthreads();
+      block_sync();
       find_digit(nb, need, sh);
       const int d = sh.digit;
       need -= sh.above;
       prefix |= static_cast<uint64_t>(d) << shift;
       mask |= static_cast<uint64_t>(nb - 1) << shift;
       const int tie = static_cast<int>(sh.hist[d]);
-      __syncthreads();
+      block_sync();
       if (tie == need) break;                 // every tying entry is taken
       if (tie <= GATHER_MAX) {
 #pragma unroll
         for (int i = 0; i < N; ++i)
           if (x[i] != 0ull && (x[i] & mask) == prefix) sh.gather[atomicAdd(&sh.gcount, 1)] = x[i];
-        __syncthreads();
+        block_sync();
         gathered = true;
         break;
       }
@@ -228,7 +228,7 @@ __device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
       if (rank < need) sh.out[atomicAdd(&sh.count, 1)] = me;
     }
   }
-  __syncthreads();
+  block_sync();
 }
 
 // cand[0..n) (distinct composites, n <= THREADS) -> sorted[rank] for the
@@ -279,7 +279,7 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
   const uint64_t sorted = warp_sort_desc(mx);
   if (lane == 7) sh.warp_thr[warp] = sorted;
   if (tid == 0) sh.gcount = 0;
-  __syncthreads();
+  block_sync();
   uint64_t thr = sh.warp_thr[0];
 #pragma unroll
   for (int w = 1; w < THREADS / 32; ++w) thr = sh.warp_thr[w] < thr ? sh.warp_thr[w] : thr;
@@ -295,13 +295,13 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
       if (pass && pos < GATHER_MAX) sh.gather[pos] = x[i];
     }
   }
-  __syncthreads();
+  block_sync();
   const int n = sh.gcount;
   if (n > GATHER_MAX) return false;
   if (tid < kPool) sh.sorted[tid] = 0ull;
-  __syncthreads();
+  block_sync();
   rank_into(sh.gather, n, sh.sorted);
-  __syncthreads();
+  block_sync();
   return true;
 }
 
@@ -330,7 +330,7 @@ __device__ __forceinline__ uint32_t block_sort_desc(uint32_t v, uint32_t (&buf)[
       uint32_t o;
       if (j >= 32) {
         buf[flip][tid] = v;
-        __syncthreads();
+        block_sync();
         o = buf[flip][tid ^ j];
         flip ^= 1;
       } else {
@@ -365,7 +365,7 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
     for (int i = 0; i + w < NI; i += 2 * w) m[i] = max(m[i], m[i + w]);
   const uint32_t T = block_sort_desc(m[0], fs.buf);
   if (tid == kPool - 1) fs.thr = T;
-  __syncthreads();
+  block_sync();
   const uint32_t thr = fs.thr;
   // held entries with key >= thr (bitwise tests: no branches)
   uint32_t cnt = 0;
@@ -378,7 +378,7 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
     if (lane >= o) incl += y;
   }
   if (lane == 31) fs.warp_cnt[warp] = incl;
-  __syncthreads();
+  block_sync();
   uint32_t off = incl - cnt, total = 0;
 #pragma unroll
   for (int w = 0; w < THREADS / 32; ++w) {
@@ -387,7 +387,7 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
     total += t;
   }
   if (total > static_cast<uint32_t>(FAST_CAP)) {
-    __syncthreads();
+    block_sync();
     return false;
   }
   if (cnt) {
@@ -397,9 +397,9 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
         fs.gather[off++] = pack_key_id(key[i], id0 + static_cast<uint32_t>(i * THREADS));
   }
   if (tid < kPool) fs.sorted[tid] = 0ull;
-  __syncthreads();
+  block_sync();
   rank_into(fs.gather, static_cast<int>(total), fs.sorted);
-  __syncthreads();
+  block_sync();
   return true;
 }
 
@@ -461,7 +461,7 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
       if (i < total) ms.in[i / kPool][i % kPool] = t[u];
     }
   }
-  __syncthreads();
+  block_sync();
   uint64_t(*src)[kPool] = ms.in;
   uint64_t(*dst)[kPool] = ms.out;
   int nl = nseg;
@@ -473,7 +473,7 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
     }
     if (nl & 1)
       for (int k = tid; k < kPool; k += THREADS) dst[pairs][k] = src[nl - 1][k];
-    __syncthreads();
+    block_sync();
     uint64_t(*t)[kPool] = src;
     src = dst;
     dst = t;
@@ -548,11 +548,11 @@ __device__ void prepare_row(const ReqDev& rq, int row, bool with_q, RowShared& r
   if (rq.pol.temperature == 0.f) return;
   const int local = row - rq.row0;
   if (tid == 0) rs.chain = 1;
-  __syncthreads();
+  block_sync();
   if (rq.parent)
     for (int j = tid; j < rq.n_nodes; j += THREADS)
       if (rq.parent[j] != j - 1) rs.chain = 0;
-  __syncthreads();
+  block_sync();
   // sampled chains take the rejection test: against the draft candidates' q
   // when given, else against q = delta(draft)
   const bool reject_row = rs.chain && local < rq.n_nodes;
@@ -565,7 +565,7 @@ __device__ void prepare_row(const ReqDev& rq, int row, bool with_q, RowShared& r
   } else if (warp == 3 && lane == 0 && reject_row) {
     rs.draft = rq.tokens[local];
   }
-  __syncthreads();
+  block_sync();
 }
 
 // The row's decisions (emit draw y, residual draw z, accept bit) once its
@@ -586,7 +586,7 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShar
   } else if (warp == 1 && reject_row && q_now) {
     build_q(rq, local, rs);
   }
-  __syncthreads();
+  block_sync();
   if (warp != 0) return;
 
   const int m = rs.m;
@@ -666,7 +666,7 @@ __device__ void prepare_accept(const ReqDev& rq, int vocab, AcceptShared& as) {
     as.bad = 0;
     as.not_chain = 0;
   }
-  __syncthreads();
+  block_sync();
   if (tid < n) {
     const int t = rq.tokens[tid];
     const int p = rq.parent ? rq.parent[tid] : tid - 1;
@@ -678,14 +678,14 @@ __device__ void prepare_accept(const ReqDev& rq, int vocab, AcceptShared& as) {
     if (p != tid - 1) atomicOr(&as.not_chain, 1);
     if (b) atomicOr(&as.bad, b);
   }
-  __syncthreads();
+  block_sync();
   const bool rejection = !greedy && !as.not_chain;
   if (rejection && rq.q_ids)
     for (int i = tid; i < n * kQCand; i += THREADS) {
       const int id = rq.q_ids[i];
       if (id < 0 || id >= vocab) atomicOr(&as.bad, VR_DEV_BAD_QID);
     }
-  __syncthreads();
+  block_sync();
 }
 
 // The acceptance walk of one request (thread 0 writes), after
@@ -696,7 +696,7 @@ __device__ void accept_request(const ReqDev& rq, const int4* dec, int32_t* statu
   const bool greedy = rq.pol.temperature == 0.f;
   const bool rejection = !greedy && !as.not_chain;
   for (int j = tid; j < R; j += THREADS) as.d[j] = __ldcg(dec + rq.row0 + j);
-  __syncthreads();
+  block_sync();
   if (tid != 0) return;
   if (as.bad) {
     set_status(status, as.bad);
@@ -782,7 +782,7 @@ __device__ __forceinline__ void sort_out_into_sorted(SelectShared& sh) {
     }
     sh.sorted[rank] = v;
   }
-  __syncthreads();
+  block_sync();
 }
 
 // The row's pool (64 composites in pool order, zero-padded) -> pool ids and
@@ -809,7 +809,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
     rs.vals[tid] = v;
   }
   if (!a.decide) return;
-  __syncthreads();
+  block_sync();
   const int b = request_of_row(tab, row);
   const ReqDev& rq = request(tab, b);
   if (!prepared) prepare_row(rq, row, true, rs);
@@ -817,10 +817,10 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
 
   // the last row of the request to finish walks the request
   __threadfence();
-  __syncthreads();
+  block_sync();
   if (tid == 0)
     last = atomicAdd(&a.req_ticket[b], 1u) == static_cast<uint32_t>(rq.n_nodes);
-  __syncthreads();
+  block_sync();
   if (!last) return;
   __threadfence();
   if (tid == 0) a.req_ticket[b] = 0u;
@@ -855,7 +855,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (a.seg_len == SEG_FAST && segment_top64_fast(rp, s0, s1, st.fast)) {
       carry = tid < kPool ? st.fast.sorted[tid] : 0ull;
       from = s1;
-      __syncthreads();
+      block_sync();
     }
     for (long long b = from; b < s1; b += SUB) {
       uint64_t x[ITEMS];
@@ -876,16 +876,16 @@ __global__ void __launch_bounds__(THREADS, 2)
         sort_out_into_sorted(sh);
       }
       carry = (tid < kPool) ? sh.sorted[tid] : 0ull;
-      __syncthreads();
+      block_sync();
     }
     if (tid < kPool) a.cand[(static_cast<size_t>(row) * a.nseg + seg) * kPool + tid] = carry;
   }
 
   // 2. the last segment of the row to finish builds the pool and decides
   __threadfence();
-  __syncthreads();
+  block_sync();
   if (tid == 0) last = atomicAdd(&a.row_ticket[row], 1u) == static_cast<uint32_t>(a.nseg - 1);
-  __syncthreads();
+  block_sync();
   if (!last) return;
   __threadfence();
   if (tid == 0) a.row_ticket[row] = 0u;
@@ -905,7 +905,7 @@ __device__ void build_row_history(const ReqDev& rq, int local, RowsShared& sr) {
   const int len = assemble_history<THREADS>(rq, local - 1, sr.H, sr.par, sr.path, &sr.h_len,
                                             &sr.h_bad);
   if (threadIdx.x == 0) sr.h_len = len < 0 ? 0 : len;
-  __syncthreads();
+  block_sync();
 }
 
 // Penalise the CTA's row in place (each distinct token of H once), refresh
@@ -930,7 +930,7 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
     if (first && t >= 0 && t < vocab) row[t] = penalize_value(__ldcg(row + t), count, pol);
   }
   __threadfence();     // the rewritten logits reach L2 before anyone reads them there
-  __syncthreads();
+  block_sync();
   // a warp per history slot: the first slot of each touched group refreshes
   // that group's maximum from the penalised row.  A warp takes eight of its
   // slots at a time and issues their loads together.
@@ -977,7 +977,7 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
     rq.q_pen[static_cast<size_t>(local) * kQCand + tid] = count ? penalize_value(x, count, pol) : x;
   }
   __threadfence();     // group maxima and q reach L2 before they are read there
-  __syncthreads();
+  block_sync();
 }
 
 // Sampling stage for rows whose group maxima (largest order key per 32
@@ -1036,7 +1036,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       best = other > best ? other : best;
     }
     if (lane == 0) sr.pool[1 + warp] = best;
-    __syncthreads();
+    block_sync();
     if (warp == 0) {
       uint64_t b = lane < THREADS / 32 ? sr.pool[1 + lane] : 0ull;
 #pragma unroll
@@ -1051,7 +1051,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       const long long id = v - lane + (ball ? __ffs(ball) - 1 : 0);
       if (lane == 0) sr.pool[0] = pack_key_id(key, static_cast<uint32_t>(id));
     }
-    __syncthreads();
+    block_sync();
     finish_row(a, tab, row, sr.pool, rs, as, last, true, 1);
     return;
   }
@@ -1082,7 +1082,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // maximum; with fewer groups every entry of every group is a candidate
   const uint32_t tau = ngroups < kPool ? 0u : static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
   if (tid == 0) sr.ccount = 0;
-  __syncthreads();
+  block_sync();
 
   // (b) the chosen groups' entries at or above tau; warp w takes groups
   // w, w + 8, ...: all of its loads are issued before any is used
@@ -1119,16 +1119,16 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (cv[t] != 0ull) sr.cands[at + __popc(ball[t] & ((1u << lane) - 1u))] = cv[t];
     at += __popc(ball[t]);
   }
-  __syncthreads();
+  block_sync();
 
   // (c) their top 64, in pool order
   const int n = sr.ccount;
   uint64_t* pool = sr.pool;
   if (n <= GATHER_MAX) {
     if (tid < kPool) pool[tid] = 0ull;
-    __syncthreads();
+    block_sync();
     rank_into(sr.cands, n, pool);
-    __syncthreads();
+    block_sync();
   } else {
     uint64_t x[C_MAX / THREADS];
 #pragma unroll
@@ -1139,7 +1139,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     block_top64(x, sh);
     sort_out_into_sorted(sh);
     if (tid < kPool) pool[tid] = sh.sorted[tid];
-    __syncthreads();
+    block_sync();
   }
   finish_row(a, tab, row, pool, rs, as, last, true);
 }

@@ -163,6 +163,15 @@ __device__ __forceinline__ float vexp(float z) {
   return __fmul_rn(p, __int_as_float((n + 127) << 23));
 }
 
+// A block barrier that every warp reaches as a whole.  __syncthreads counts
+// arrivals per warp, so lanes that branched apart just before (one lane
+// walking a loop while the others skip it) must reconverge first; a barrier
+// reached by a warp in pieces can release before the late lanes arrive.
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // penalty history ("Speculative decoding on RDNA" §04): H[0..len) = the last
 // W = pol.window tokens of (hist || tokens on the path root -> end_node),
@@ -178,7 +187,7 @@ __device__ int assemble_history(const ReqDev& rq, int end_node, int32_t* H, int3
                                 int32_t* path, int* n_s, int* bad_s) {
   const int tid = threadIdx.x, nn = rq.n_nodes;
   for (int j = tid; j < nn; j += NT) par[j] = rq.parent ? rq.parent[j] : j - 1;
-  __syncthreads();
+  block_sync();
   if (tid == 0) {
     int n = 0, node = end_node, bad = 0;
     while (node >= 0) {
@@ -197,14 +206,14 @@ __device__ int assemble_history(const ReqDev& rq, int end_node, int32_t* H, int3
     *n_s = n;
     *bad_s = bad;
   }
-  __syncthreads();
+  block_sync();
   const int bad = *bad_s;
   const int from_path = bad ? 0 : min(*n_s, rq.pol.window);
   const int from_hist = bad ? 0 : min(rq.hist_len, rq.pol.window - from_path);
   for (int i = tid; i < from_hist; i += NT) H[i] = rq.hist[rq.hist_len - from_hist + i];
   // path[] is leaf-first
   for (int i = tid; i < from_path; i += NT) H[from_hist + i] = rq.tokens[path[from_path - 1 - i]];
-  __syncthreads();
+  block_sync();
   return bad ? -1 : from_hist + from_path;
 }
 
