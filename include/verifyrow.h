@@ -219,9 +219,13 @@ VR_API int vr_topk(const float* x, int rows, int vocab, int k, int32_t* ids, flo
  *     contents; calls that overlap on the GPU race on it, so the caller must
  *     serialise them (one stream, one thread at a time);
  *   - the first call on each device looks the array's address up on that
- *     device (cudaGetSymbolAddress, the device must be current); make that
- *     first call before any stream capture on the device.
- * Allocates nothing (no cudaMalloc or cudaFree, on any call).
+ *     device (cudaGetSymbolAddress, the device must be current).  Under
+ *     CUDA's lazy module loading (the default) that lookup is also what
+ *     places the array, about 1 MiB, and the select's kernel code in that
+ *     device's memory, so the device footprint grows once, at the first
+ *     call.  Make that first call at start-up, before any stream capture on
+ *     the device; later calls leave the device's free memory unchanged.
+ * Calls no cudaMalloc, cudaFree or allocating library routine, on any call.
  */
 #define VR_NOALLOC_SELECT_MAX_ROWS 32
 VR_API int vr_verify_select_noalloc(const float* logits, int rows, int vocab, int32_t* pool_ids,
