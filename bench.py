@@ -34,6 +34,14 @@ WEIGHT_BYTES = V * H * 2
 METRIC = "verify windows/s (hidden 4096, V=151936, k+1 rows); HBM GB/s vs 8 TB/s peak"
 WORKLOAD = "sampled chain: hidden 4096, vocab 151936, k=3 (4 rows), T 0.7, top-k 20, min-p 0.05, top-p 0.95"
 POLICY = dict(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95)
+# windows behind each breakdown of the line (stages, latency, other
+# workloads, host-buffer paths); fixed so that a short --steps run still
+# reports figures over large samples
+STAGE_SAMPLES = 2000
+LATENCY_SAMPLES = 500
+EXTRA_SAMPLES = 1000
+E2E_SAMPLES = 2000
+E2E_SYNC_SAMPLES = 1000
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -588,35 +596,38 @@ def main():
     ws = vb.workspace(ROWS, H, V, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def window(i, path=vb.VR_PATH_AUTO):
-        s = i % N_WINDOWS
-        vb.verify_window(wd, win["act"][s], win["drafts"][s], pol, s, 4096, logits, out, acc, ne, ws,
-                         q_ids=win["q_ids"][s], q_logits=win["q_log"][s], path=path, stream=stream)
+    # each distinct window's call, marshalled once (vb.prepare_window): a
+    # timed window costs one C call on the host
+    calls = [vb.prepare_window(wd, win["act"][s], win["drafts"][s], pol, s, 4096, logits, out, acc,
+                               ne, ws, q_ids=win["q_ids"][s], q_logits=win["q_log"][s],
+                               stream=stream) for s in range(N_WINDOWS)]
 
-    for i in range(args.warmup):
-        window(i)
-    torch.cuda.synchronize(dev)
-    if vb.device_status(ws) != 0:
-        raise RuntimeError("device status set during warm-up")
+    def window(i):
+        calls[i % N_WINDOWS]()
 
     # ---- timed region: K fused windows ----
+    # The clock sampler starts before the warm-up, so the GPU does not sit
+    # idle (and its clocks do not fall back) between the warm-up and the
+    # timed region.
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    replicas.barrier()
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        for i in range(args.warmup):
+            window(i)
+        replicas.barrier()
+        torch.cuda.synchronize(dev)
         e0.record(stream)
         for i in range(args.steps):
             window(i)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-    replicas.barrier()
+        replicas.barrier()
     elapsed_s = e0.elapsed_time(e1) / 1000.0
     job_s, job_windows = replicas.job_time_and_units(elapsed_s, args.steps,
                                                      device=dev if args.gpus > 1 else None)
     value = job_windows / job_s
     if vb.device_status(ws) != 0:
-        raise RuntimeError("device status set during the timed region")
+        raise RuntimeError("device status set during the warm-up or the timed region")
 
     if args.mode == "window":
         if rank == 0:
@@ -627,7 +638,8 @@ def main():
 
     # ---- stage breakdown: the same windows through the stage entry points,
     # events between stages on the launching stream ----
-    n_stage = min(args.steps, 2000)
+    # sample sizes of the breakdowns below are fixed, whatever --steps is
+    n_stage = STAGE_SAMPLES
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_stage)]
     pool_ids = torch.empty((ROWS, 64), dtype=torch.int32, device=dev)
     torch.cuda.synchronize(dev)
@@ -643,10 +655,12 @@ def main():
     proj_ms = [e[0].elapsed_time(e[1]) for e in evs]
     samp_ms = [e[1].elapsed_time(e[2]) for e in evs]
     proj_avg_s = statistics.fmean(proj_ms) / 1000.0
+    proj_sorted = sorted(proj_ms)
+    proj_pct = lambda q: 1000.0 * proj_sorted[min(len(proj_sorted) - 1, int(q * len(proj_sorted)))]
     # per-window latency of the fused call: events around every window, so
     # no window overlaps the next (the timed region above lets them overlap
     # their launch and prologue)
-    n_lat = min(args.steps, 500)
+    n_lat = LATENCY_SAMPLES
     lat_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_lat)]
     torch.cuda.synchronize(dev)
     for i in range(n_lat):
@@ -690,7 +704,7 @@ def main():
             sweep[name][str(R)] = round(1000.0 * t0.elapsed_time(t1) / n_it, 2)
 
     extra = None if args.no_extra else extra_workloads(torch, vb, synth, wd, dev, stream,
-                                                       min(args.steps, 1000))
+                                                       EXTRA_SAMPLES)
     cost_model = None if args.no_extra else window_cost_model(torch, vb, synth, wd, dev, stream)
 
     # ---- e2e: host inputs -> window -> host outputs, through the C ABI ----
@@ -708,7 +722,7 @@ def main():
     h_out = pin(np.zeros(ROWS, np.int32))
     h_res = [pin(np.zeros(ROWS + 2, np.int32)) for _ in range(2)]
     events = [torch.cuda.Event() for _ in range(2)]
-    n_e2e = min(args.steps, 2000)
+    n_e2e = E2E_SAMPLES
 
     def e2e_async(n, first):
         emitted = 0
@@ -736,15 +750,16 @@ def main():
     replicas.barrier()
     e2e_job_s, e2e_units = replicas.job_time_and_units(e2e_s, n_e2e,
                                                        device=dev if args.gpus > 1 else None)
+    host_calls = [vb.prepare_window_host(wd, h_act[s], h_dr[s], pol, s, 4096, logits, h_out, ws,
+                                         q_ids_h=h_qi[s], q_logits_h=h_ql[s], stream=stream)
+                  for s in range(N_WINDOWS)]
     for i in range(10):
-        vb.verify_window_host(wd, h_act[i], h_dr[i], pol, i, 4096, logits, h_out, ws,
-                              q_ids_h=h_qi[i], q_logits_h=h_ql[i], stream=stream)
-    n_sync = min(args.steps, 1000)
+        host_calls[i]()
+    n_sync = E2E_SYNC_SAMPLES
     t0 = time.perf_counter()
     for i in range(n_sync):
-        s = i % N_WINDOWS
-        vb.verify_window_host(wd, h_act[s], h_dr[s], pol, s, 4096, logits, h_out, ws,
-                              q_ids_h=h_qi[s], q_logits_h=h_ql[s], stream=stream)
+        if host_calls[i % N_WINDOWS]()[1] < 1:
+            raise RuntimeError("a window emitted nothing")
     sync_s = time.perf_counter() - t0
     h2d = ROWS * H * 4 + K_DRAFTS * 4 + K_DRAFTS * 8 * 4 * 2
     d2h = (ROWS + 2) * 4
@@ -764,7 +779,10 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "projection (project_tc_kernel, planes built in the kernel)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_record("project_tc_kernel"),
-                     "algorithmic_bytes_per_launch": WEIGHT_BYTES},
+                     "algorithmic_bytes_per_launch": WEIGHT_BYTES,
+                     "launches_timed": n_stage,
+                     "launch_us": {"mean": 1e6 * proj_avg_s, "p10": proj_pct(0.10),
+                                   "p50": proj_pct(0.50), "p90": proj_pct(0.90)}},
         "stages_us": {"projection": 1000.0 * statistics.fmean(proj_ms),
                       "pool_policy_accept": 1000.0 * statistics.fmean(samp_ms),
                       "pool_select_only": select_us,
@@ -784,7 +802,7 @@ def main():
                 "the host link by the staging kernel and [accept, n, ids] written back into "
                 "pinned memory by the acceptance kernel (no copy-engine transfers)"},
         "e2e_sync": {"value": n_sync / sync_s, "unit": "windows/s",
-                     "api": "vr_verify_window_host, one wait per window"},
+                     "api": "vr_verify_window_host (prepared call), one wait per window"},
         # per timed window: project_tc (planes built in the kernel for <= 16
         # rows) and sample_rows; no penalties in this workload, so no penalty
         # or q-copy launches

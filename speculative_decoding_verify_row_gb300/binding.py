@@ -292,9 +292,8 @@ def verify_sample_accept(pen_logits, tokens, policy, seed, position, out_ids, ou
            "vr_verify_sample_accept")
 
 
-def verify_window(weight, act, tokens, policy, seed, position, logits, out_ids, out_accept,
-                  out_n, ws, parent=None, q_ids=None, q_logits=None, hist=None, pen_logits=None,
-                  path=VR_PATH_AUTO, stream=None):
+def _window_args(weight, act, tokens, policy, seed, position, logits, out_ids, out_accept,
+                 out_n, ws, parent, q_ids, q_logits, hist, pen_logits, path, stream):
     V, H = weight.shape
     R = act.shape[0]
     n = R - 1
@@ -307,14 +306,41 @@ def verify_window(weight, act, tokens, policy, seed, position, logits, out_ids, 
     _dev(out_accept, torch.int32, "out_accept", (1,))
     _dev(out_n, torch.int32, "out_n", (1,))
     pol = policy.c()
-    _check(lib().vr_verify_window(_ptr(weight), _ptr(act), R, H, V, path,
-                                  _opt_i32(tokens, "tokens", (n,)), _opt_i32(parent, "parent", (n,)),
-                                  n, _opt_i32(q_ids, "q_ids", (n, VR_QCAND)), _ptr(q_logits),
-                                  _opt_i32(hist, "hist"), 0 if hist is None else hist.numel(),
-                                  ctypes.byref(pol), seed, position, _ptr(logits),
-                                  _ptr(pen_logits), _ptr(out_ids), _ptr(out_accept), _ptr(out_n),
-                                  _ptr(ws), ws.numel(), _stream(stream, act.device)),
-           "vr_verify_window")
+    return pol, (_ptr(weight), _ptr(act), R, H, V, path, _opt_i32(tokens, "tokens", (n,)),
+                 _opt_i32(parent, "parent", (n,)), n, _opt_i32(q_ids, "q_ids", (n, VR_QCAND)),
+                 _ptr(q_logits), _opt_i32(hist, "hist"), 0 if hist is None else hist.numel(),
+                 ctypes.byref(pol), seed, position, _ptr(logits), _ptr(pen_logits),
+                 _ptr(out_ids), _ptr(out_accept), _ptr(out_n), _ptr(ws), ws.numel(),
+                 _stream(stream, act.device))
+
+
+def verify_window(weight, act, tokens, policy, seed, position, logits, out_ids, out_accept,
+                  out_n, ws, parent=None, q_ids=None, q_logits=None, hist=None, pen_logits=None,
+                  path=VR_PATH_AUTO, stream=None):
+    _, args = _window_args(weight, act, tokens, policy, seed, position, logits, out_ids,
+                           out_accept, out_n, ws, parent, q_ids, q_logits, hist, pen_logits, path,
+                           stream)
+    _check(lib().vr_verify_window(*args), "vr_verify_window")
+
+
+def prepare_window(weight, act, tokens, policy, seed, position, logits, out_ids, out_accept,
+                   out_n, ws, parent=None, q_ids=None, q_logits=None, hist=None, pen_logits=None,
+                   path=VR_PATH_AUTO, stream=None):
+    """verify_window with its arguments checked and marshalled once: returns
+    a callable that enqueues that same window (same buffers, seed, position
+    and stream) each time it is called, at the cost of one C call.  For a
+    loop that reuses its buffers; the tensors must outlive the callable."""
+    pol, args = _window_args(weight, act, tokens, policy, seed, position, logits, out_ids,
+                             out_accept, out_n, ws, parent, q_ids, q_logits, hist, pen_logits,
+                             path, stream)
+    fn = lib().vr_verify_window
+
+    def call(_keep=(pol, weight, act, tokens, logits, out_ids, out_accept, out_n, ws, parent,
+                    q_ids, q_logits, hist, pen_logits)):
+        st = fn(*args)
+        if st != VR_OK:
+            raise VerifyRowError(st, "vr_verify_window")
+    return call
 
 
 def make_request(n_nodes, tokens, policy, seed, position, out_ids, out_accept, out_n,
@@ -368,33 +394,63 @@ def _pinned_head():
     return head
 
 
-def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
-                       ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
-                       pen_logits=None, path=VR_PATH_AUTO, stream=None):
-    """The window with host inputs and outputs (pinned host tensors are read
-    and written by the kernels directly, pageable ones copied).  Returns
-    (accept, n_emitted); synchronises."""
+def _window_host_args(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h, ws,
+                      parent_h, q_ids_h, q_logits_h, hist_h, pen_logits, path, stream, head):
     V, H = weight.shape
     R = act_h.shape[0]
     n = R - 1
     _dev(weight, _WEIGHT_DTYPES, "weight")
     _dev(logits, torch.float32, "logits", (R, V))
     _dev(pen_logits, torch.float32, "pen_logits", (R, V))
-    head, head_np = _pinned_head()
     pol = policy.c()
-    _check(lib().vr_verify_window_host(_ptr(weight), _host_ptr(act_h, torch.float32, "act_h"), R, H,
-                                       V, path, _host_ptr(tokens_h, torch.int32, "tokens_h"),
-                                       _host_ptr(parent_h, torch.int32, "parent_h"), n,
-                                       _host_ptr(q_ids_h, torch.int32, "q_ids_h"),
-                                       _host_ptr(q_logits_h, torch.float32, "q_logits_h"),
-                                       _host_ptr(hist_h, torch.int32, "hist_h"),
-                                       0 if hist_h is None else hist_h.numel(), ctypes.byref(pol),
-                                       seed, position, _ptr(logits), _ptr(pen_logits),
-                                       _host_ptr(out_ids_h, torch.int32, "out_ids_h"),
-                                       ctypes.c_void_p(head.data_ptr()),
-                                       ctypes.c_void_p(head.data_ptr() + 4), _ptr(ws), ws.numel(),
-                                       _stream(stream, logits.device)), "vr_verify_window_host")
+    return pol, (_ptr(weight), _host_ptr(act_h, torch.float32, "act_h"), R, H, V, path,
+                 _host_ptr(tokens_h, torch.int32, "tokens_h"),
+                 _host_ptr(parent_h, torch.int32, "parent_h"), n,
+                 _host_ptr(q_ids_h, torch.int32, "q_ids_h"),
+                 _host_ptr(q_logits_h, torch.float32, "q_logits_h"),
+                 _host_ptr(hist_h, torch.int32, "hist_h"), 0 if hist_h is None else hist_h.numel(),
+                 ctypes.byref(pol), seed, position, _ptr(logits), _ptr(pen_logits),
+                 _host_ptr(out_ids_h, torch.int32, "out_ids_h"), ctypes.c_void_p(head.data_ptr()),
+                 ctypes.c_void_p(head.data_ptr() + 4), _ptr(ws), ws.numel(),
+                 _stream(stream, logits.device))
+
+
+def verify_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
+                       ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
+                       pen_logits=None, path=VR_PATH_AUTO, stream=None):
+    """The window with host inputs and outputs (pinned host tensors are read
+    and written by the kernels directly, pageable ones copied).  Returns
+    (accept, n_emitted); synchronises."""
+    head, head_np = _pinned_head()
+    _, args = _window_host_args(weight, act_h, tokens_h, policy, seed, position, logits,
+                                out_ids_h, ws, parent_h, q_ids_h, q_logits_h, hist_h, pen_logits,
+                                path, stream, head)
+    _check(lib().vr_verify_window_host(*args), "vr_verify_window_host")
     return int(head_np[0]), int(head_np[1])
+
+
+def prepare_window_host(weight, act_h, tokens_h, policy, seed, position, logits, out_ids_h,
+                        ws, parent_h=None, q_ids_h=None, q_logits_h=None, hist_h=None,
+                        pen_logits=None, path=VR_PATH_AUTO, stream=None):
+    """verify_window_host with its arguments checked and marshalled once:
+    returns a callable that runs that window (reading the host inputs as
+    they are at the time of the call) and returns (accept, n_emitted), one C
+    call and one wait each time.  The accept/n_emitted pair lives in a
+    pinned pair owned by the callable; the tensors must outlive it."""
+    head = torch.zeros(2, dtype=torch.int32).pin_memory()
+    head_np = head.numpy()
+    pol, args = _window_host_args(weight, act_h, tokens_h, policy, seed, position, logits,
+                                  out_ids_h, ws, parent_h, q_ids_h, q_logits_h, hist_h,
+                                  pen_logits, path, stream, head)
+    fn = lib().vr_verify_window_host
+
+    def call(_keep=(pol, head, weight, act_h, tokens_h, logits, out_ids_h, ws, parent_h, q_ids_h,
+                    q_logits_h, hist_h, pen_logits)):
+        st = fn(*args)
+        if st != VR_OK:
+            raise VerifyRowError(st, "vr_verify_window_host")
+        return int(head_np[0]), int(head_np[1])
+    return call
 
 
 def verify_window_host_async(weight, act_h, tokens_h, policy, seed, position, logits, out_h,
