@@ -118,7 +118,7 @@ typedef struct vr_request {
   vr_policy policy;
   uint64_t seed;            /* request seed of the random stream              */
   uint64_t position;        /* |prompt || emitted| at the window start        */
-  int32_t* out_ids;         /* [n_nodes + 1] emitted ids                      */
+  int32_t* out_ids;         /* [n_nodes + 1] emitted ids first; later entries unspecified */
   int32_t* out_accept;      /* [1] accepted drafts                            */
   int32_t* out_n_emitted;   /* [1] emitted ids (accepted + 1; 0 on error)     */
 } vr_request;
@@ -271,8 +271,9 @@ VR_API int vr_verify_policy(const float* pool_vals, int rows, int pool_len, cons
  * key = (seed, 0)) word 0 >> 40, times 2^-24 (a float32); purpose 1 = accept
  * uniform, 2 = emitted draw; t = u * S picks the first j whose running sum
  * exceeds t.  The probabilities, accept test and residual are float32.
- * Outputs: out_ids [n_nodes + 1] (emitted ids, then untouched), out_accept,
- * out_n_emitted (= accepted + 1 >= 1; 0 if the device status was set).
+ * Outputs: out_ids [n_nodes + 1] (the emitted ids first; the entries after
+ * them hold unspecified values), out_accept, out_n_emitted (= accepted + 1
+ * >= 1; 0 if the device status was set).
  */
 VR_API int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab, const int32_t* tokens,
                             const int32_t* parent, int n_nodes, const int32_t* q_ids,
@@ -335,7 +336,8 @@ VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int
  * Inputs and arguments as in vr_verify_window_host.  The call stages the
  * inputs into ws as vr_verify_window_host does, enqueues the window and
  * returns.  out_h receives (2 + rows) int32: out_h[0] = accept,
- * out_h[1] = n_emitted, out_h[2 .. 2 + n_emitted) = the emitted ids.
+ * out_h[1] = n_emitted, out_h[2 .. 2 + n_emitted) = the emitted ids (the
+ * entries after them hold unspecified values).
  * Ownership and lifetime (all caller-owned):
  *   - out_h should be pinned (page-locked) host memory: the acceptance writes
  *     it directly (a pageable out_h gets one asynchronous copy); it is valid

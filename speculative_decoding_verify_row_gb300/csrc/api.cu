@@ -17,8 +17,12 @@ constexpr size_t kAlign = 256;
 // sampling kernel (which leaves them at zero after every call)
 constexpr size_t kRowTicketOff = 256;
 constexpr size_t kReqTicketOff = kRowTicketOff + VR_MAX_ROWS * 4;
+// then one 64-bit word per request: the done and accept bits of the rows of a
+// chain (the acceptance without a walk)
+constexpr size_t kReqMaskOff = kReqTicketOff + VR_MAX_REQUESTS * 4;
 constexpr size_t kControlBytes = 8192;
-static_assert(kReqTicketOff + VR_MAX_REQUESTS * 4 <= kControlBytes, "control region");
+static_assert(kReqMaskOff % 8 == 0, "control region alignment");
+static_assert(kReqMaskOff + VR_MAX_REQUESTS * 8 <= kControlBytes, "control region");
 
 struct Layout {
   size_t status, planes, cand, gmax, pool_ids, pool_vals, dec, q_pen, reqs, row_req;
@@ -164,18 +168,29 @@ bool records_gmax(int path, int vocab) {
          sample_rows_supported(vocab);
 }
 
+// True when the row sampling kernel after a projection on `path` starts long
+// before its wait returns: its CTAs, two per SM, fit on the SMs the
+// tensor-core projection leaves free.  It may then warm its instruction
+// cache before the wait.
+bool row_kernel_starts_early(int path, int rows, int vocab) {
+  if (path != VR_PATH_AUTO && path != VR_PATH_TC) return false;
+  return (rows + 1) / 2 <= tc_free_sms(rows, vocab);
+}
+
 // penalties -> pool + policy -> acceptance, for requests already in `tab`;
-// gmax: the group maxima of `target` if the projection recorded them
+// gmax: the group maxima of `target` if the projection recorded them; early:
+// row_kernel_starts_early for the projection that ran
 int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* target,
-                  uint32_t* gmax, bool any_active, bool any_q, void* ws, const Layout& L,
-                  cudaStream_t s) {
+                  uint32_t* gmax, bool any_active, bool any_q, bool early, void* ws,
+                  const Layout& L, cudaStream_t s) {
   (void)n_req;
   // windows on a tensor-core path: the row kernel applies the penalties itself
   if (gmax)
     return launch_sample_rows(target, rows, vocab, gmax, at<uint32_t>(ws, L.status + kReqTicketOff),
+                              at<unsigned long long>(ws, L.status + kReqMaskOff),
                               at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
                               at<int4>(ws, L.dec), at<int32_t>(ws, L.status),
-                              any_active && any_q, any_active ? target : nullptr, s);
+                              any_active && any_q, any_active ? target : nullptr, early, s);
   int st;
   if (any_active) {
     st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);
@@ -183,7 +198,8 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
   }
   return launch_sample(target, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
-                       at<uint32_t>(ws, L.status + kReqTicketOff), at<int32_t>(ws, L.pool_ids),
+                       at<uint32_t>(ws, L.status + kReqTicketOff),
+                       at<unsigned long long>(ws, L.status + kReqMaskOff), at<int32_t>(ws, L.pool_ids),
                        at<float>(ws, L.pool_vals), &tab, at<int4>(ws, L.dec),
                        at<int32_t>(ws, L.status), s);
 }
@@ -204,7 +220,8 @@ int window_device(const uint16_t* weight, const float* act, int rows, int hidden
   float* q_pen = (act_pen && q_ids) ? at<float>(ws, L.q_pen) : const_cast<float*>(q_logits);
   const ReqTable tab = single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, q_pen, hist,
                                        hist_len, pol, seed, position, out_ids, out_accept, out_n));
-  return sample_stages(tab, 1, rows, vocab, target, gmax, act_pen, q_ids != nullptr, ws, L, s);
+  return sample_stages(tab, 1, rows, vocab, target, gmax, act_pen, q_ids != nullptr,
+                       row_kernel_starts_early(path, rows, vocab), ws, L, s);
 }
 
 }  // namespace
@@ -282,7 +299,8 @@ int vr_verify_select(const float* logits, int rows, int vocab, int32_t* pool_ids
   const Layout L = layout(rows, 8, vocab);
   return launch_sample(logits, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
-                       at<uint32_t>(ws, L.status + kReqTicketOff), pool_ids, pool_vals, nullptr,
+                       at<uint32_t>(ws, L.status + kReqTicketOff), nullptr, pool_ids, pool_vals,
+                       nullptr,
                        nullptr, at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream));
 }
 
@@ -295,7 +313,8 @@ int vr_topk(const float* x, int rows, int vocab, int k, int32_t* ids, float* val
   const Layout L = layout(rows, 8, vocab);
   return launch_sample(x, rows, vocab, at<uint64_t>(ws, L.cand),
                        at<uint32_t>(ws, L.status + kRowTicketOff),
-                       at<uint32_t>(ws, L.status + kReqTicketOff), ids, vals, nullptr, nullptr,
+                       at<uint32_t>(ws, L.status + kReqTicketOff), nullptr, ids, vals, nullptr,
+                       nullptr,
                        at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), k);
 }
 
@@ -324,7 +343,7 @@ int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab, const 
       single(make_req(0, n_nodes, tokens, parent, q_ids, q_logits, const_cast<float*>(q_logits),
                       nullptr, 0, *policy, seed, position, out_ids, out_accept, out_n_emitted));
   return sample_stages(tab, 1, rows, vocab, const_cast<float*>(pen_logits), nullptr, false, false,
-                       ws, L, static_cast<cudaStream_t>(stream));
+                       false, ws, L, static_cast<cudaStream_t>(stream));
 }
 
 int vr_verify_window(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
@@ -400,7 +419,8 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
   tab.many = at<ReqDev>(ws, L.reqs);
   tab.row_req = at<int32_t>(ws, L.row_req);
   tab.n_req = n_req;
-  return sample_stages(tab, n_req, rows, vocab, target, gmax, any_active, any_q, ws, L, s);
+  return sample_stages(tab, n_req, rows, vocab, target, gmax, any_active, any_q,
+                       row_kernel_starts_early(path, rows, vocab), ws, L, s);
 }
 
 }  // extern "C"

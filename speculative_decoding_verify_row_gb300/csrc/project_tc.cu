@@ -567,6 +567,30 @@ size_t tc_scratch_bytes(int rows, int hidden) {
   return groups * tc::BN * h * 2;                                   // the planes
 }
 
+namespace {
+
+// One CTA per SM; or, when fewer CTAs take the same number of units each and
+// the SMs this leaves free can hold the row sampling kernel that follows in a
+// window (one CTA per row, two per SM), that smaller grid: the sampling
+// kernel then sits beside the projection, and the next window's projection
+// CTAs all start on SMs of their own.
+int tc_grid(int rows, int vocab, int num_sms) {
+  const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
+  const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
+  int grid = std::min(n_units, num_sms);
+  const int per_cta = (n_units + num_sms - 1) / num_sms;
+  const int balanced = (n_units + per_cta - 1) / per_cta;
+  if ((rows + 1) / 2 <= num_sms - balanced) grid = balanced;
+  return grid;
+}
+
+}  // namespace
+
+int tc_free_sms(int rows, int vocab) {
+  const int num_sms = device_sm_count();
+  return num_sms > 0 ? num_sms - tc_grid(rows, vocab, num_sms) : 0;
+}
+
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, float* logits2, void* scratch, uint32_t* gmax,
                       int32_t* status, cudaStream_t stream) {
@@ -575,17 +599,7 @@ int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hi
   CUtensorMap tm_w;
   // one 256-row box per unit and K block (both vocab tiles of the unit)
   if (!encode_bf16_tile(&tm_w, weight, hidden, vocab, tc::BK, tc::MT * tc::BM)) return VR_ERR_ARG;
-  const int n_mtiles = (vocab + tc::BM - 1) / tc::BM;
-  const int n_units = (n_mtiles + tc::MT - 1) / tc::MT;
-  // One CTA per SM; or, when fewer CTAs take the same number of units each
-  // and the SMs this leaves free can hold the row sampling kernel that
-  // follows in a window (one CTA per row, two per SM), that smaller grid:
-  // the sampling kernel then sits beside the projection, and the next
-  // window's projection CTAs all start on SMs of their own.
-  int grid = std::min(n_units, num_sms);
-  const int per_cta = (n_units + num_sms - 1) / num_sms;
-  const int balanced = (n_units + per_cta - 1) / per_cta;
-  if ((rows + 1) / 2 <= num_sms - balanced) grid = balanced;
+  const int grid = tc_grid(rows, vocab, num_sms);
 
   if (rows <= tc::FUSED_MAX_ROWS) {
     // one group, planes built in the kernel from the activations

@@ -88,6 +88,7 @@ struct RowsShared {
   uint64_t cands[C_MAX];
   uint64_t pool[kPool];
   int ccount;
+
   // the row's penalty history (built before the wait)
   int32_t H[VR_MAX_PENALTY_WINDOW];
   int32_t par[VR_MAX_WINDOW_ROWS];
@@ -108,11 +109,17 @@ struct RowShared {
   int m, qm, chain, acc;
   int32_t draft;
   float S, qS, u1, u2;
+  ReqDev req;     // the row's request (load_request), read from here
+  int req_b;      // its index in the request table
+  int4 dec;       // the row's decisions, as written to dec[row]
+  uint32_t acc_bits;   // chains: the accept bits of every row of the request
 };
 
 struct AcceptShared {
   int32_t tok[MAXR], par[MAXR];
   int4 d[MAXR];
+  int32_t depth[MAXR];       // greedy tree walk: each node's depth and
+  uint8_t ok[MAXR];          // whether its whole path agrees
   int bad, not_chain;
 };
 
@@ -485,6 +492,28 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
 // ---------------------------------------------------------------------------
 // per-row decisions
 
+// Copy the request of `row`, and its index, into rs.req / rs.req_b: one
+// round of loads by the first warp.  Every later read of a request field is
+// then a shared-memory read, not a dependent load from the kernel's
+// parameter buffer or the workspace (each of those cost a memory latency
+// when first touched after the wait).  Ends with a block barrier.
+__device__ __forceinline__ void load_request(const ReqTable& tab, int row, RowShared& rs) {
+  constexpr int W = static_cast<int>(sizeof(ReqDev) / 4);
+  static_assert(sizeof(ReqDev) % 4 == 0 && W <= 64, "request copy");
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int b = request_of_row(tab, row);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&request(tab, b));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&rs.req);
+    const uint32_t w0 = src[tid];
+    const uint32_t w1 = tid + 32 < W ? src[tid + 32] : 0u;
+    if (tid < W) dst[tid] = w0;
+    if (tid + 32 < W) dst[tid + 32] = w1;
+    if (tid == 0) rs.req_b = b;
+  }
+  block_sync();
+}
+
 __device__ __forceinline__ int last_positive(const float* w, int m) {
   const int lane = threadIdx.x & 31;
   uint32_t b = __ballot_sync(0xffffffffu, lane + 32 < m && w[lane + 32] > 0.0f);
@@ -571,12 +600,16 @@ __device__ void prepare_row(const ReqDev& rq, int row, bool with_q, RowShared& r
 // The row's decisions (emit draw y, residual draw z, accept bit) once its
 // pool is known; prepare_row ran before, with q built there unless q_now.
 __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShared& rs,
-                           int4* dec) {
+                           int4* dec, bool live = true) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const vr_policy& pol = rq.pol;
   const int local = row - rq.row0;
   if (pol.temperature == 0.f) {
-    if (tid == 0) dec[row] = make_int4(rs.ids[0], rs.ids[0], rs.ids[0], 0);
+    if (tid == 0) {
+      const int4 d = make_int4(rs.ids[0], rs.ids[0], rs.ids[0], 0);
+      if (live) dec[row] = d;
+      rs.dec = d;
+    }
     return;
   }
   const bool reject_row = rs.chain && local < rq.n_nodes;
@@ -649,7 +682,11 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShar
       z = rs.ids[jz];
     }
   }
-  if (lane == 0) dec[row] = make_int4(rs.ids[0], y, z, acc);
+  if (lane == 0) {
+    const int4 d = make_int4(rs.ids[0], y, z, acc);
+    if (live) dec[row] = d;
+    rs.dec = d;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -708,8 +745,8 @@ __device__ void accept_request(const ReqDev& rq, const int4* dec, int32_t* statu
   const int4* d = as.d;
   int accepted = 0;
   if (greedy) {
-    bool ok[MAXR];
-    int depth[MAXR];
+    uint8_t* ok = as.ok;       // in shared memory, not in the thread's local memory
+    int32_t* depth = as.depth;
     int best = -1, best_depth = 0;
     for (int j = 0; j < n; ++j) {
       const int p = as.par[j];
@@ -759,6 +796,7 @@ struct SampleArgs {
   uint64_t* cand;          // [rows][nseg][64]
   uint32_t* row_ticket;    // [rows], zero between calls
   uint32_t* req_ticket;    // [requests], zero between calls
+  unsigned long long* req_mask;  // [requests] chain done/accept bits, zero between calls
   int32_t* pool_ids;       // [rows][out_k]
   float* pool_vals;        // [rows][out_k]
   int out_k;               // leading pool entries written per row (<= 64)
@@ -767,6 +805,7 @@ struct SampleArgs {
   int decide;              // 0: pools only
   int q_after_wait;        // q logits penalised in this window (built after the wait)
   float* pen_logits;       // row kernel: penalties applied in place here (== logits), or null
+  int warm;                // row kernel: run the instruction warm-up pass before the wait
 };
 
 // sh.out[0..count) -> sh.sorted in pool order (zero-padded)
@@ -787,10 +826,11 @@ __device__ __forceinline__ void sort_out_into_sorted(SelectShared& sh) {
 
 // The row's pool (64 composites in pool order, zero-padded) -> pool ids and
 // values, then the row's decisions, then (last row of its request) the
-// acceptance walk.
+// acceptance.  live == false: the row kernel's instruction warm-up pass,
+// which writes nothing outside shared memory and stops after the decisions.
 __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, const uint64_t* pool,
                            RowShared& rs, AcceptShared& as, int& last, bool prepared,
-                           int n_pool = kPool) {
+                           int n_pool = kPool, bool live = true) {
   const int tid = threadIdx.x;
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const int n = min(a.vocab, n_pool);
@@ -801,7 +841,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
       id = static_cast<int32_t>(packed_id(pool[tid]));
       v = value_of_key(static_cast<uint32_t>(pool[tid] >> 32), rp, id);
     }
-    if (tid < a.out_k) {
+    if (live && tid < a.out_k) {
       a.pool_ids[static_cast<size_t>(row) * a.out_k + tid] = id;
       a.pool_vals[static_cast<size_t>(row) * a.out_k + tid] = v;
     }
@@ -810,10 +850,64 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
   }
   if (!a.decide) return;
   block_sync();
-  const int b = request_of_row(tab, row);
-  const ReqDev& rq = request(tab, b);
+  if (!prepared) load_request(tab, row, rs);
+  const ReqDev& rq = rs.req;
+  const int b = rs.req_b;
   if (!prepared) prepare_row(rq, row, true, rs);
-  decide_row(rq, row, n, prepared && a.q_after_wait, rs, a.dec);
+  decide_row(rq, row, n, prepared && a.q_after_wait, rs, a.dec, live);
+  if (!live) return;
+
+  // Chains of at most 32 rows: no walk.  Each row writes its own output slot
+  // (a draft row: its draft if it accepts it, else its replacement token (the
+  // residual draw, or the argmax for greedy requests); the last row: its
+  // bonus), then ORs its done bit (1 << local) and its accept bit
+  // (<< 32 + local) into the request's word.  The CTA whose OR completes the
+  // done bits holds every accept bit in the returned word: the accepted
+  // prefix is the leading run of ones, and the slots up to it are already
+  // written.  Slots past the emitted ones hold later rows' tokens.
+  const int local = row - rq.row0;
+  const int R = rq.n_nodes + 1;
+  const bool greedy = rq.pol.temperature == 0.f;
+  if (a.req_mask && R <= 32 && (!rq.parent || (!greedy && rs.chain))) {
+    block_sync();       // rs.dec, written by warp 0
+    if (tid == 0) {
+      const int4 d = rs.dec;
+      int bit = 0;
+      int32_t tok = d.y;                         // the last row: its bonus draw
+      if (greedy) {
+        tok = d.x;                               // the argmax is the draft when it accepts
+        bit = local < rq.n_nodes && (prepared ? as.tok[local] : rq.tokens[local]) == d.x;
+      } else if (local < rq.n_nodes) {
+        bit = d.w;
+        tok = bit ? rs.draft : d.z;
+      }
+      rq.out_ids[local] = tok;
+      const unsigned long long mine =
+          (1ull << local) | (static_cast<unsigned long long>(bit) << (32 + local));
+      const unsigned long long all = atomicOr(&a.req_mask[b], mine) | mine;
+      const uint32_t full = R == 32 ? 0xffffffffu : ((1u << R) - 1u);
+      last = static_cast<uint32_t>(all) == full;
+      rs.acc_bits = static_cast<uint32_t>(all >> 32);
+    }
+    block_sync();
+    if (!last) return;
+    if (tid == 0) a.req_mask[b] = 0ull;
+    if (!prepared) prepare_accept(rq, a.vocab, as);
+    if (tid == 0) {
+      if (as.bad) {
+        set_status(a.status, as.bad);
+        *rq.out_accept = 0;
+        *rq.out_n = 0;
+      } else {
+        const uint32_t rej = ~rs.acc_bits;       // the first row that did not accept
+        const int lead = rej ? __ffs(static_cast<int>(rej)) - 1 : 32;
+        const int accepted = lead < rq.n_nodes ? lead : rq.n_nodes;
+        *rq.out_accept = accepted;
+        *rq.out_n = accepted + 1;
+      }
+    }
+    return;
+  }
 
   // the last row of the request to finish walks the request
   __threadfence();
@@ -990,158 +1084,197 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
 //      gathered and their top 64 taken;
 //  (c) pool, policy, decisions and acceptance as in sample_kernel.
 __global__ void __launch_bounds__(THREADS, 2)
-    sample_rows_kernel(const __grid_constant__ SampleArgs a, const __grid_constant__ ReqTable tab,
-                       uint32_t* __restrict__ gmax, int ngroups) {
+    sample_rows_kernel(const __grid_constant__ SampleArgs args,
+                       const __grid_constant__ ReqTable tab, uint32_t* __restrict__ gmax,
+                       int ngroups) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   RowsShared& sr = *reinterpret_cast<RowsShared*>(dyn_smem);
   SelectShared& sh = sr.sel;
   __shared__ RowShared rs;
   __shared__ AcceptShared as;
   __shared__ int last;
+  __shared__ SampleArgs s_args;
   pdl_trigger();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // before the wait: everything of the row's decision that needs no logits
   // (this kernel only runs after the window's first kernel, which triggers
-  // its dependents only once its own predecessors are complete)
-  const ReqDev& rq0 = request(tab, request_of_row(tab, row));
+  // its dependents only once its own predecessors are complete).  First the
+  // kernel's arguments and the row's request go to shared memory, so that
+  // no read of theirs after the wait goes to memory.
+  {
+    constexpr int W = static_cast<int>(sizeof(SampleArgs) / 4);
+    static_assert(sizeof(SampleArgs) % 4 == 0 && W <= 64, "argument copy");
+    if (warp == 1) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(&args);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(&s_args);
+      const uint32_t w0 = src[lane];
+      const uint32_t w1 = lane + 32 < W ? src[lane + 32] : 0u;
+      if (lane < W) dst[lane] = w0;
+      if (lane + 32 < W) dst[lane + 32] = w1;
+    }
+  }
+  load_request(tab, row, rs);
+  const SampleArgs& a = s_args;
+  const ReqDev& rq0 = rs.req;
   const bool pen = a.pen_logits && penalties_active(rq0.pol);
   prepare_row(rq0, row, !a.q_after_wait, rs);
   prepare_accept(rq0, a.vocab, as);
   if (pen) build_row_history(rq0, row - rq0.row0, sr);
-  pdl_wait();
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
-  if (pen) {
-    if (sr.h_bad && tid == 0) set_status(a.status, VR_DEV_BAD_PARENT);
-    penalize_own_row(rq0, row - rq0.row0, a.pen_logits + static_cast<size_t>(row) * a.vocab,
-                     a.vocab, gmax + static_cast<size_t>(row) * ngroups, sr);
-  }
 
-  if (rq0.pol.temperature == 0.f) {
-    // a greedy request needs only each row's argmax: the largest key among
-    // the group maxima, the lowest group holding it, and the lowest id of
-    // that key inside the group (the pool's first entry; no other entry is
-    // formed)
-    uint64_t best = 0ull;
-#pragma unroll
-    for (int i = 0; i < GI_MAX; ++i) {
-      const int g = i * THREADS + tid;
-      const uint32_t k = __ldcg(gm + (g < ngroups ? g : 0));   // unconditional: loads overlap
-      const uint64_t c = g < ngroups ? pack_key_id(k, static_cast<uint32_t>(g)) : 0ull;
-      best = c > best ? c : best;
+  // The body below runs twice, as a loop (one copy of its instructions).
+  // Pass 0, before the wait, works on the logits and group maxima as they
+  // stand (the previous window's, or values being overwritten) and writes
+  // nothing outside shared memory: it only brings this code into the SM's
+  // instruction cache.  Every phase runs once per launch, so on cold code
+  // each waited on instruction fetches (a phase ran up to twice as long as
+  // warm).  Pass 1 runs after the wait, on the window's logits.  The host
+  // asks for pass 0 (a.warm) only when the kernel's CTAs fit on the SMs the
+  // projection leaves free, i.e. when they start long before the wait
+  // returns; otherwise they start as the projection ends, and pass 0 would
+  // only delay them.
+#pragma unroll 1
+  for (int pass = a.warm ? 0 : 1; pass < 2; ++pass) {
+    const bool live = pass == 1;
+    if (live) pdl_wait();
+    if (live && pen) {
+      if (sr.h_bad && tid == 0) set_status(a.status, VR_DEV_BAD_PARENT);
+      penalize_own_row(rq0, row - rq0.row0, a.pen_logits + static_cast<size_t>(row) * a.vocab,
+                       a.vocab, gmax + static_cast<size_t>(row) * ngroups, sr);
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    if (lane == 0) sr.pool[1 + warp] = best;
-    block_sync();
-    if (warp == 0) {
-      uint64_t b = lane < THREADS / 32 ? sr.pool[1 + lane] : 0ull;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, b, o);
-        b = other > b ? other : b;
-      }
-      const uint32_t key = static_cast<uint32_t>(b >> 32);
-      const long long v = static_cast<long long>(packed_id(b)) * 32 + lane;
-      const uint32_t kv = float_key(__ldcg(rp + (v < a.vocab ? v : 0)));
-      const uint32_t ball = __ballot_sync(0xffffffffu, v < a.vocab && kv == key);
-      const long long id = v - lane + (ball ? __ffs(ball) - 1 : 0);
-      if (lane == 0) sr.pool[0] = pack_key_id(key, static_cast<uint32_t>(id));
-    }
-    block_sync();
-    finish_row(a, tab, row, sr.pool, rs, as, last, true, 1);
-    return;
-  }
 
-  // (a) top 64 groups, as composites (max key << 32) | ~group
-  const uint64_t* chosen = sr.fast.sorted;
-  {
-    uint32_t gk[GI_MAX];
-#pragma unroll
-    for (int i = 0; i < GI_MAX; ++i) {
-      const int g = i * THREADS + tid;
-      gk[i] = __ldcg(gm + (g < ngroups ? g : 0));     // unconditional: loads overlap
-    }
-    if (!keys_top64(gk, ngroups - tid, static_cast<uint32_t>(tid), sr.fast)) {
-      uint64_t x[GI_MAX];
-#pragma unroll
+    if (rq0.pol.temperature == 0.f) {
+      // a greedy request needs only each row's argmax: the largest key among
+      // the group maxima, the lowest group holding it, and the lowest id of
+      // that key inside the group (the pool's first entry; no other entry is
+      // formed)
+      uint64_t best = 0ull;
+  #pragma unroll
       for (int i = 0; i < GI_MAX; ++i) {
         const int g = i * THREADS + tid;
-        x[i] = g < ngroups ? pack_key_id(gk[i], static_cast<uint32_t>(g)) : 0ull;
+        const uint32_t k = __ldcg(gm + (g < ngroups ? g : 0));   // unconditional: loads overlap
+        const uint64_t c = g < ngroups ? pack_key_id(k, static_cast<uint32_t>(g)) : 0ull;
+        best = c > best ? c : best;
+      }
+  #pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if (lane == 0) sr.pool[1 + warp] = best;
+      block_sync();
+      if (warp == 0) {
+        uint64_t b = lane < THREADS / 32 ? sr.pool[1 + lane] : 0ull;
+  #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const uint64_t other = __shfl_xor_sync(0xffffffffu, b, o);
+          b = other > b ? other : b;
+        }
+        const uint32_t key = static_cast<uint32_t>(b >> 32);
+        const long long v = static_cast<long long>(packed_id(b)) * 32 + lane;
+        const uint32_t kv = float_key(__ldcg(rp + (v < a.vocab ? v : 0)));
+        const uint32_t ball = __ballot_sync(0xffffffffu, v < a.vocab && kv == key);
+        const long long id = v - lane + (ball ? __ffs(ball) - 1 : 0);
+        if (lane == 0) sr.pool[0] = pack_key_id(key, static_cast<uint32_t>(id));
+      }
+      block_sync();
+      finish_row(a, tab, row, sr.pool, rs, as, last, true, 1, live);
+      continue;
+    }
+
+    // (a) the 64 groups with the largest maxima, as composites
+    // (max key << 32) | ~group, and (b) their entries at or above the 64th
+    // maximum
+    {
+      uint32_t gk[GI_MAX];
+  #pragma unroll
+      for (int i = 0; i < GI_MAX; ++i) {
+        const int g = i * THREADS + tid;
+        gk[i] = __ldcg(gm + (g < ngroups ? g : 0));     // unconditional: loads overlap
+      }
+      const uint64_t* chosen = sr.fast.sorted;
+      if (!keys_top64(gk, ngroups - tid, static_cast<uint32_t>(tid), sr.fast)) {
+        uint64_t x[GI_MAX];
+  #pragma unroll
+        for (int i = 0; i < GI_MAX; ++i) {
+          const int g = i * THREADS + tid;
+          x[i] = g < ngroups ? pack_key_id(gk[i], static_cast<uint32_t>(g)) : 0ull;
+        }
+        block_top64(x, sh);
+        sort_out_into_sorted(sh);
+        chosen = sh.sorted;
+      }
+      const int nchosen = ngroups < kPool ? ngroups : kPool;
+      // 64 chosen groups hold at least 64 entries at or above the 64th group
+      // maximum; with fewer groups every entry of every group is a candidate
+      const uint32_t tau =
+          ngroups < kPool ? 0u : static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
+      if (tid == 0) sr.ccount = 0;
+      block_sync();
+      // the chosen groups' entries at or above tau; warp w takes groups
+      // w, w + 8, ...: all of its loads are issued before any is used
+      constexpr int GPW = kPool / (THREADS / 32);     // groups per warp
+      float fv[GPW];
+  #pragma unroll
+      for (int t = 0; t < GPW; ++t) {
+        const int j = warp + t * (THREADS / 32);
+        const long long v =
+            static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
+        fv[t] = __ldcg(rp + (v < a.vocab ? v : 0));       // unconditional: loads overlap
+      }
+      uint32_t kv[GPW];
+  #pragma unroll
+      for (int t = 0; t < GPW; ++t) kv[t] = float_key(fv[t]);
+      // one slot reservation per warp for all of its groups
+      uint64_t cv[GPW];
+      uint32_t ball[GPW];
+      int total = 0;
+  #pragma unroll
+      for (int t = 0; t < GPW; ++t) {
+        const int j = warp + t * (THREADS / 32);
+        const long long v =
+            static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
+        uint64_t c = 0ull;
+        if (j < nchosen && v < a.vocab && kv[t] >= tau)
+          c = pack_key_id(kv[t], static_cast<uint32_t>(v));
+        cv[t] = c;
+        ball[t] = __ballot_sync(0xffffffffu, c != 0ull);
+        total += __popc(ball[t]);
+      }
+      int at = 0;
+      if (lane == 0 && total) at = atomicAdd(&sr.ccount, total);
+      at = __shfl_sync(0xffffffffu, at, 0);
+  #pragma unroll
+      for (int t = 0; t < GPW; ++t) {
+        if (cv[t] != 0ull) sr.cands[at + __popc(ball[t] & ((1u << lane) - 1u))] = cv[t];
+        at += __popc(ball[t]);
+      }
+      block_sync();
+    }
+
+    // (c) their top 64, in pool order
+    const int n = sr.ccount;
+    uint64_t* pool = sr.pool;
+    if (n <= GATHER_MAX) {
+      if (tid < kPool) pool[tid] = 0ull;
+      block_sync();
+      rank_into(sr.cands, n, pool);
+      block_sync();
+    } else {
+      uint64_t x[C_MAX / THREADS];
+  #pragma unroll
+      for (int i = 0; i < C_MAX / THREADS; ++i) {
+        const int k = i * THREADS + tid;
+        x[i] = k < n ? sr.cands[k] : 0ull;
       }
       block_top64(x, sh);
       sort_out_into_sorted(sh);
-      chosen = sh.sorted;
+      if (tid < kPool) pool[tid] = sh.sorted[tid];
+      block_sync();
     }
+    finish_row(a, tab, row, pool, rs, as, last, true, kPool, live);
   }
-  const int nchosen = ngroups < kPool ? ngroups : kPool;
-  // 64 chosen groups hold at least 64 entries at or above the 64th group
-  // maximum; with fewer groups every entry of every group is a candidate
-  const uint32_t tau = ngroups < kPool ? 0u : static_cast<uint32_t>(chosen[nchosen - 1] >> 32);
-  if (tid == 0) sr.ccount = 0;
-  block_sync();
-
-  // (b) the chosen groups' entries at or above tau; warp w takes groups
-  // w, w + 8, ...: all of its loads are issued before any is used
-  constexpr int GPW = kPool / (THREADS / 32);     // groups per warp
-  float fv[GPW];
-#pragma unroll
-  for (int t = 0; t < GPW; ++t) {
-    const int j = warp + t * (THREADS / 32);
-    const long long v = static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
-    fv[t] = __ldcg(rp + (v < a.vocab ? v : 0));       // unconditional: loads overlap
-  }
-  uint32_t kv[GPW];
-#pragma unroll
-  for (int t = 0; t < GPW; ++t) kv[t] = float_key(fv[t]);
-  // one slot reservation per warp for all of its groups
-  uint64_t cv[GPW];
-  uint32_t ball[GPW];
-  int total = 0;
-#pragma unroll
-  for (int t = 0; t < GPW; ++t) {
-    const int j = warp + t * (THREADS / 32);
-    const long long v = static_cast<long long>(packed_id(chosen[j < nchosen ? j : 0])) * 32 + lane;
-    uint64_t c = 0ull;
-    if (j < nchosen && v < a.vocab && kv[t] >= tau) c = pack_key_id(kv[t], static_cast<uint32_t>(v));
-    cv[t] = c;
-    ball[t] = __ballot_sync(0xffffffffu, c != 0ull);
-    total += __popc(ball[t]);
-  }
-  int at = 0;
-  if (lane == 0 && total) at = atomicAdd(&sr.ccount, total);
-  at = __shfl_sync(0xffffffffu, at, 0);
-#pragma unroll
-  for (int t = 0; t < GPW; ++t) {
-    if (cv[t] != 0ull) sr.cands[at + __popc(ball[t] & ((1u << lane) - 1u))] = cv[t];
-    at += __popc(ball[t]);
-  }
-  block_sync();
-
-  // (c) their top 64, in pool order
-  const int n = sr.ccount;
-  uint64_t* pool = sr.pool;
-  if (n <= GATHER_MAX) {
-    if (tid < kPool) pool[tid] = 0ull;
-    block_sync();
-    rank_into(sr.cands, n, pool);
-    block_sync();
-  } else {
-    uint64_t x[C_MAX / THREADS];
-#pragma unroll
-    for (int i = 0; i < C_MAX / THREADS; ++i) {
-      const int k = i * THREADS + tid;
-      x[i] = k < n ? sr.cands[k] : 0ull;
-    }
-    block_top64(x, sh);
-    sort_out_into_sorted(sh);
-    if (tid < kPool) pool[tid] = sh.sorted[tid];
-    block_sync();
-  }
-  finish_row(a, tab, row, pool, rs, as, last, true);
 }
 
 __global__ void policy_kernel(const float* __restrict__ pool_vals, int pool_len, vr_policy pol,
@@ -1191,8 +1324,9 @@ size_t select_cand_bytes(int rows, int vocab) {
 }
 
 int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
-                  uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
-                  int4* dec, int32_t* status, cudaStream_t stream, int out_k) {
+                  uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
+                  float* pool_vals, const ReqTable* tab, int4* dec, int32_t* status,
+                  cudaStream_t stream, int out_k) {
   if (out_k < 1 || out_k > kPool) return VR_ERR_ARG;
   const int nseg = select_segments(vocab);
   smp::SampleArgs a;
@@ -1203,6 +1337,7 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.cand = cand;
   a.row_ticket = row_ticket;
   a.req_ticket = req_ticket;
+  a.req_mask = req_mask;
   a.pool_ids = pool_ids;
   a.pool_vals = pool_vals;
   a.out_k = out_k;
@@ -1227,13 +1362,14 @@ bool sample_rows_supported(int vocab) {
 }
 
 int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
-                       uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
-                       const ReqTable& tab, int4* dec, int32_t* status, bool q_after_wait,
-                       float* pen_logits, cudaStream_t stream) {
+                       uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
+                       float* pool_vals, const ReqTable& tab, int4* dec, int32_t* status,
+                       bool q_after_wait, float* pen_logits, bool warm, cudaStream_t stream) {
   smp::SampleArgs a{};
   a.logits = logits;
   a.vocab = vocab;
   a.req_ticket = req_ticket;
+  a.req_mask = req_mask;
   a.pool_ids = pool_ids;
   a.pool_vals = pool_vals;
   a.out_k = kPool;
@@ -1242,6 +1378,7 @@ int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
   a.decide = 1;
   a.q_after_wait = q_after_wait ? 1 : 0;
   a.pen_logits = pen_logits;
+  a.warm = warm ? 1 : 0;
   const size_t smem = sizeof(smp::RowsShared);
   static std::atomic<bool> attr_set[kMaxDevices];
   if (set_smem_limit_once(smp::sample_rows_kernel, static_cast<int>(smem), attr_set) != cudaSuccess)

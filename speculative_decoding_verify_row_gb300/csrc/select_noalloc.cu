@@ -72,5 +72,5 @@ extern "C" int vr_verify_select_noalloc(const float* logits, int rows, int vocab
   if (cudaMemsetAsync(counters, 0, VR_NOALLOC_SELECT_MAX_ROWS * sizeof(uint32_t), s) != cudaSuccess)
     return VR_ERR_CUDA;
   return vr::launch_sample(logits, rows, vocab, scratch + vr::kCounterSlots, counters, nullptr,
-                           pool_ids, pool_vals, nullptr, nullptr, nullptr, s);
+                           nullptr, pool_ids, pool_vals, nullptr, nullptr, nullptr, s);
 }

@@ -260,26 +260,20 @@ __device__ __forceinline__ int warp_first(int m, Pred pred) {
 // c past N is not written.
 template <int N>
 __device__ __forceinline__ void running_sums_n(const float* w, float* c, int n) {
-  float v[N];
-#pragma unroll
-  for (int j = 0; j < N; j += 4) {
-    const float4 t = *reinterpret_cast<const float4*>(w + j);
-    v[j] = t.x;
-    v[j + 1] = t.y;
-    v[j + 2] = t.z;
-    v[j + 3] = t.w;
-  }
+  // one 16-byte chunk at a time, no array: every value stays in a register
+  // (a whole-row array was placed in local memory)
   float acc = 0.0f;
 #pragma unroll
   for (int j = 0; j < N; j += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(w + j);
     float4 o;
-    acc = __fadd_rn(acc, j < n ? v[j] : 0.0f);
+    acc = __fadd_rn(acc, j < n ? t.x : 0.0f);
     o.x = acc;
-    acc = __fadd_rn(acc, j + 1 < n ? v[j + 1] : 0.0f);
+    acc = __fadd_rn(acc, j + 1 < n ? t.y : 0.0f);
     o.y = acc;
-    acc = __fadd_rn(acc, j + 2 < n ? v[j + 2] : 0.0f);
+    acc = __fadd_rn(acc, j + 2 < n ? t.z : 0.0f);
     o.z = acc;
-    acc = __fadd_rn(acc, j + 3 < n ? v[j + 3] : 0.0f);
+    acc = __fadd_rn(acc, j + 3 < n ? t.w : 0.0f);
     o.w = acc;
     *reinterpret_cast<float4*>(c + j) = o;
   }

@@ -72,6 +72,9 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
 // scratch (tc_scratch_bytes, 16-byte aligned): the activation planes for
 // more than 16 rows, else room for an aligned copy of act
 size_t tc_scratch_bytes(int rows, int hidden);
+// SMs the tensor-core projection of `rows` rows leaves free (its grid may
+// leave room for the row sampling kernel that follows it in a window)
+int tc_free_sms(int rows, int vocab);
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, float* logits2, void* scratch, uint32_t* gmax,
                       int32_t* status, cudaStream_t stream);
@@ -86,27 +89,33 @@ int launch_penalize(const ReqTable& tab, int rows_total, float* logits, int voca
 // sampling stage, one kernel: logits [rows][vocab] -> pool ids/vals
 // [rows][64]; with a request table also the policy, the per-row decisions
 // dec[row] = (argmax, emit draw y, residual draw z, accept bit) and the
-// acceptance walk of every request.  row_ticket [rows] and req_ticket
-// [requests] must be zero on entry and are zero again on exit.
+// acceptance of every request (a walk over the rows' decisions, or for
+// chains of at most 32 rows the per-request done/accept bits in req_mask).
+// row_ticket [rows], req_ticket and req_mask [requests] must be zero on
+// entry and are zero again on exit.
 int select_segments(int vocab);
 size_t select_cand_bytes(int rows, int vocab);
 // out_k: entries written per row to pool_ids/pool_vals (row stride out_k);
 // the decisions always use the whole 64-wide pool.
 int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint32_t* row_ticket,
-                  uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals, const ReqTable* tab,
+                  uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
+                  float* pool_vals, const ReqTable* tab,
                   int4* dec, int32_t* status, cudaStream_t stream, int out_k = kPool);
 
 // the same stage for rows whose group maxima gmax [rows][ceil(vocab/32)]
 // (largest order key per 32 vocabulary rows) are known: one CTA per row
 bool sample_rows_supported(int vocab);
 // q_after_wait: some request's draft logits are penalised in this window, so
-// q is built after the wait.  pen_logits (== logits, or null): the kernel
+// q is built after the wait.  warm: the kernel's CTAs start well before its
+// wait returns (they fit beside the projection), so it first runs its body
+// once without effect to load its instructions.  pen_logits (== logits, or null): the kernel
 // applies each active request's penalties to its own rows there first (and
 // refreshes gmax), so no penalty kernel runs before it.
 int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
-                       uint32_t* req_ticket, int32_t* pool_ids, float* pool_vals,
+                       uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
+                       float* pool_vals,
                        const ReqTable& tab, int4* dec, int32_t* status, bool q_after_wait,
-                       float* pen_logits, cudaStream_t stream);
+                       float* pen_logits, bool warm, cudaStream_t stream);
 
 int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
                   int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream);
