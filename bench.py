@@ -57,12 +57,16 @@ def parse_args():
     p.add_argument("--no-extra", action="store_true",
                    help="skip the penalised-chain, tree and batched workloads")
     p.add_argument("--mode", choices=["full", "window", "project", "project_batched", "batched",
-                                      "topk"],
+                                      "topk", "penalize"],
                    default="full",
                    help="window: only the timed windows (for a profiler's launch list); "
                         "project: only the projection of one window (for a kernel capture); "
                         "project_batched: only the 256-row batched projection at hidden 5120; "
-                        "topk: only the batched top-K (15 x 248320, K 16)")
+                        "topk: only the batched top-K (15 x 248320, K 16); "
+                        "penalize: only the penalty entry point on the penalised chain's rows")
+    p.add_argument("--path", choices=["tc", "ffma"], default="tc",
+                   help="projection path of --mode project")
+    p.add_argument("--rows", type=int, default=ROWS, help="rows of --mode project")
     return p.parse_args()
 
 
@@ -500,18 +504,49 @@ def run_topk_only(torch, vb, dev, args):
 
 
 def run_projection_only(torch, vb, synth, wd, dev, args):
-    """The projection of one 4-row window, warm-up + steps times."""
-    a = torch.from_numpy(synth.activations(ROWS, H, 0)).to(dev)
-    lg = torch.empty((ROWS, V), dtype=torch.float32, device=dev)
-    ws = vb.workspace(ROWS, H, V, device=dev)
+    """The projection of one window (--rows rows, --path), warm-up + steps
+    times."""
+    R = args.rows
+    path = vb.VR_PATH_FFMA if args.path == "ffma" else vb.VR_PATH_TC
+    a = torch.from_numpy(synth.activations(R, H, 0)).to(dev)
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    ws = vb.workspace(R, H, V, device=dev)
     for _ in range(args.warmup):
-        vb.verify_project(wd, a, lg, ws)
+        vb.verify_project(wd, a, lg, ws, path=path)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vb.verify_project(wd, a, lg, ws)
+        vb.verify_project(wd, a, lg, ws, path=path)
     torch.cuda.synchronize(dev)
-    print(json.dumps({"mode": "project", "steps": args.steps,
+    print(json.dumps({"mode": "project", "path": args.path, "rows": R, "steps": args.steps,
+                      "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
+
+
+def run_penalize_only(torch, vb, synth, wd, dev, args):
+    """The penalty entry point on the penalised chain's rows (k 8, 9 rows,
+    4096-token history, W 64, repeat 1.1, presence 1.5, frequency 0.2,
+    draft candidates penalised too), warm-up + steps times on the logits of
+    one projection (each call penalises the rows again: the same work)."""
+    k, R = 8, 9
+    pol = vb.Policy(temperature=0.7, top_k=0, min_p=0.05, top_p=0.95, repeat=1.1, presence=1.5,
+                    frequency=0.2, window=64)
+    rng = np.random.default_rng(100)
+    a = torch.from_numpy(synth.activations(R, H, 100)).to(dev)
+    lg = torch.empty((R, V), dtype=torch.float32, device=dev)
+    ws = vb.workspace(R, H, V, device=dev)
+    vb.verify_project(wd, a, lg, ws)
+    d = torch.from_numpy(rng.integers(0, V, k).astype(np.int32)).to(dev)
+    q = torch.from_numpy(rng.integers(0, V, (k, 8)).astype(np.int32)).to(dev)
+    ql = torch.from_numpy(rng.standard_normal((k, 8)).astype(np.float32)).to(dev)
+    h = torch.from_numpy(synth.zipf_history(4096, V, seed=100)).to(dev)
+    for _ in range(args.warmup):
+        vb.verify_penalize(lg, d, h, pol, ws, q_ids=q, q_logits=ql)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vb.verify_penalize(lg, d, h, pol, ws, q_ids=q, q_logits=ql)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"mode": "penalize", "rows": R, "steps": args.steps,
                       "us_per_call": 1e6 * (time.perf_counter() - t0) / max(1, args.steps)}))
 
 
@@ -586,6 +621,9 @@ def main():
     wd = torch.from_numpy(W.view(np.int16)).to(dev)
     if args.mode == "project":
         run_projection_only(torch, vb, synth, wd, dev, args)
+        return
+    if args.mode == "penalize":
+        run_penalize_only(torch, vb, synth, wd, dev, args)
         return
     win = make_windows(torch, vb, synth, wd, dev)
     pol = vb.Policy(**POLICY)
