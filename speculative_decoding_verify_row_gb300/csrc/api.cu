@@ -168,13 +168,13 @@ bool records_gmax(int path, int vocab) {
          sample_rows_supported(vocab);
 }
 
-// True when the row sampling kernel after a projection on `path` starts long
-// before its wait returns: its CTAs, two per SM, fit on the SMs the
-// tensor-core projection leaves free.  It may then warm its instruction
-// cache before the wait.
+// True when the row sampling kernel after a projection on `path` starts well
+// before its wait returns: its CTAs, two per SM, fit on the SMs that the
+// tensor-core projection leaves free from its start or frees a unit of work
+// before its end.  It may then warm its instruction cache before the wait.
 bool row_kernel_starts_early(int path, int rows, int vocab) {
   if (path != VR_PATH_AUTO && path != VR_PATH_TC) return false;
-  return (rows + 1) / 2 <= tc_free_sms(rows, vocab);
+  return (rows + 1) / 2 <= tc_early_free_sms(rows, vocab);
 }
 
 // penalties -> pool + policy -> acceptance, for requests already in `tab`;

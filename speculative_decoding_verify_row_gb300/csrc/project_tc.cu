@@ -586,9 +586,14 @@ int tc_grid(int rows, int vocab, int num_sms) {
 
 }  // namespace
 
-int tc_free_sms(int rows, int vocab) {
+int tc_early_free_sms(int rows, int vocab) {
   const int num_sms = device_sm_count();
-  return num_sms > 0 ? num_sms - tc_grid(rows, vocab, num_sms) : 0;
+  if (num_sms <= 0) return 0;
+  const int grid = tc_grid(rows, vocab, num_sms);
+  const int n_units = ((vocab + tc::BM - 1) / tc::BM + tc::MT - 1) / tc::MT;
+  const int per_cta = (n_units + grid - 1) / grid;
+  // SMs without a CTA, plus the CTAs with one unit fewer than the others
+  return (num_sms - grid) + (grid * per_cta - n_units);
 }
 
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,

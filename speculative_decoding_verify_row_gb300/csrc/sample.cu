@@ -725,15 +725,42 @@ __device__ void prepare_accept(const ReqDev& rq, int vocab, AcceptShared& as) {
   block_sync();
 }
 
-// The acceptance walk of one request (thread 0 writes), after
+// The acceptance walk of one request (warp 0; lane 0 writes), after
 // prepare_accept, with every row's decisions in dec.
 __device__ void accept_request(const ReqDev& rq, const int4* dec, int32_t* status,
                                AcceptShared& as) {
-  const int n = rq.n_nodes, R = n + 1, tid = threadIdx.x;
+  const int n = rq.n_nodes, R = n + 1, tid = threadIdx.x, lane = tid & 31;
   const bool greedy = rq.pol.temperature == 0.f;
   const bool rejection = !greedy && !as.not_chain;
   for (int j = tid; j < R; j += THREADS) as.d[j] = __ldcg(dec + rq.row0 + j);
   block_sync();
+  if (tid >= 32) return;
+  if (!greedy && !rejection && !as.bad) {
+    // naive sampling descent: from the root, emit the current row's draw y and
+    // move to the lowest-index child of the current node carrying y; one
+    // ballot over the (at most 63) nodes finds it
+    int32_t* out = rq.out_ids;
+    int cur = -1, cnt = 0;
+    while (true) {
+      const int32_t y = as.d[cur < 0 ? 0 : 1 + cur].y;
+      if (lane == 0) out[cnt] = y;
+      ++cnt;
+      const int j0 = lane, j1 = lane + 32;
+      const bool m0 = j0 < n && as.par[j0] == cur && as.tok[j0] == y;
+      const bool m1 = j1 < n && as.par[j1] == cur && as.tok[j1] == y;
+      const uint32_t b0 = __ballot_sync(0xffffffffu, m0);
+      const uint32_t b1 = __ballot_sync(0xffffffffu, m1);
+      const int next = b0 ? __ffs(static_cast<int>(b0)) - 1
+                          : (b1 ? 32 + __ffs(static_cast<int>(b1)) - 1 : -1);
+      if (next < 0) break;
+      cur = next;
+    }
+    if (lane == 0) {
+      *rq.out_accept = cnt - 1;
+      *rq.out_n = cnt;
+    }
+    return;
+  }
   if (tid != 0) return;
   if (as.bad) {
     set_status(status, as.bad);
@@ -767,21 +794,6 @@ __device__ void accept_request(const ReqDev& rq, const int4* dec, int32_t* statu
     for (int i = 0; i < a; ++i) out[i] = as.tok[i];
     out[a] = (a < n) ? d[a].z : d[n].y;
     accepted = a;
-  } else {
-    int cur = -1, cnt = 0;
-    while (true) {
-      const int32_t y = d[cur < 0 ? 0 : 1 + cur].y;
-      out[cnt++] = y;
-      int next = -1;
-      for (int j = cur + 1; j < n; ++j)
-        if (as.par[j] == cur && as.tok[j] == y) {
-          next = j;
-          break;
-        }
-      if (next < 0) break;
-      cur = next;
-    }
-    accepted = cnt - 1;
   }
   *rq.out_accept = accepted;
   *rq.out_n = accepted + 1;

@@ -72,9 +72,11 @@ int launch_project_tcb(const uint16_t* weight, const float* act, int rows, int h
 // scratch (tc_scratch_bytes, 16-byte aligned): the activation planes for
 // more than 16 rows, else room for an aligned copy of act
 size_t tc_scratch_bytes(int rows, int hidden);
-// SMs the tensor-core projection of `rows` rows leaves free (its grid may
-// leave room for the row sampling kernel that follows it in a window)
-int tc_free_sms(int rows, int vocab);
+// SMs that the tensor-core projection of `rows` rows leaves free, at its
+// start or at least one unit of work before its end (its grid may leave room
+// for the row sampling kernel that follows it in a window, and CTAs with one
+// unit fewer than the others end early)
+int tc_early_free_sms(int rows, int vocab);
 int launch_project_tc(const uint16_t* weight, const float* act, int rows, int hidden, int vocab,
                       float* logits, float* logits2, void* scratch, uint32_t* gmax,
                       int32_t* status, cudaStream_t stream);
