@@ -315,12 +315,15 @@ VR_API int vr_verify_window_batched(const uint16_t* weight, const float* act, in
  * NULL), q_ids_h/q_logits_h (or NULL), hist_h [hist_len] are host pointers;
  * the last min(hist_len, VR_MAX_PENALTY_WINDOW) history tokens are used.
  * weight, logits and pen_logits are device pointers.  The inputs go into ws:
- * when every input buffer is pinned (page-locked, so mapped into the device's
- * address space) a staging kernel reads them directly, otherwise they are
- * copied.  Then the window runs; pinned output buffers (out_ids_h [rows], and
- * out_accept_h with out_n_emitted_h) are written by the kernel, pageable ones
- * copied back; the call SYNCHRONISES the stream before returning (one wait
- * per call).
+ * when every input buffer is device-accessible a staging kernel reads them
+ * directly, otherwise they are copied.  Device-accessible means pinned
+ * (page-locked, mapped into the device's address space), or any host buffer
+ * on a device that reads host memory through the host's page tables
+ * (cudaDevAttrPageableMemoryAccessUsesHostPageTables, e.g. Grace systems;
+ * there no buffer is queried per call).  Then the window runs; device-
+ * accessible output buffers (out_ids_h [rows], and out_accept_h with
+ * out_n_emitted_h) are written by the kernel, others copied back; the call
+ * SYNCHRONISES the stream before returning (one wait per call).
  */
 VR_API int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, int hidden,
                           int vocab, int path, const int32_t* tokens_h, const int32_t* parent_h,

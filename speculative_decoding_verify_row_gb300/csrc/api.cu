@@ -1,6 +1,7 @@
 // C ABI of libverifyrow: argument validation, workspace layout and the
 // order of launches of each entry point.  See include/verifyrow.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -427,11 +428,37 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
 
 namespace {
 
-// The device address of a pinned (page-locked, device-mapped) host buffer,
-// or nullptr when the buffer is pageable (then it is copied instead).
+// True when kernels on the current device can read and write any host
+// address through the host's page tables (a coherent CPU-GPU system such as
+// Grace with ATS): then every host buffer is device-accessible at its own
+// address, pinned or not.  Looked up once per device.
+bool host_pages_device_visible() {
+  static std::atomic<int> state[kMaxDevices];     // 0 unknown, 1 no, 2 yes
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached) {
+    const int v = state[dev].load(std::memory_order_acquire);
+    if (v) return v == 2;
+  }
+  int attr = 0;
+  const bool yes = cudaDeviceGetAttribute(&attr, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                                          dev) == cudaSuccess &&
+                   attr != 0;
+  if (!yes) cudaGetLastError();
+  if (cached) state[dev].store(yes ? 2 : 1, std::memory_order_release);
+  return yes;
+}
+
+// The device address of a host buffer that kernels may read and write: with
+// `direct` (the caller waits for the window before returning, and host pages
+// are device-visible) the buffer itself, with no driver query per call;
+// else the mapping of a pinned (page-locked, device-mapped) buffer, or
+// nullptr when the buffer is pageable (then it is copied instead).
 template <class T>
-T* mapped(T* p) {
+T* mapped(T* p, bool direct = false) {
   if (!p) return nullptr;
+  if (direct) return p;
   cudaPointerAttributes a{};
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
@@ -450,7 +477,7 @@ int window_host_enqueue(const uint16_t* weight, const float* act_h, int rows, in
                         const int32_t* hist_h, int hist_len, const vr_policy* policy,
                         uint64_t seed, uint64_t position, float* logits, float* pen_logits,
                         void* ws, size_t ws_bytes, cudaStream_t s, int32_t* ids_dst,
-                        int32_t* accept_dst, int32_t* n_dst) {
+                        int32_t* accept_dst, int32_t* n_dst, bool direct) {
   const Layout L = layout(rows, hidden, vocab);
   const int h_keep = std::min(hist_len, VR_MAX_PENALTY_WINDOW);
   const int32_t* hist_tail = h_keep > 0 ? hist_h + (hist_len - h_keep) : nullptr;
@@ -470,7 +497,7 @@ int window_host_enqueue(const uint16_t* weight, const float* act_h, int rows, in
   bool all_mapped = true;
   for (const In& x : in) {
     if (!x.h || x.words == 0) continue;
-    const void* m = mapped(x.h);
+    const void* m = mapped(x.h, direct);
     if (!m) {
       all_mapped = false;
       break;
@@ -529,14 +556,17 @@ int vr_verify_window_host(const uint16_t* weight, const float* act_h, int rows, 
   int32_t* out = at<int32_t>(ws, layout(rows, hidden, vocab).st_out);
   // pinned output buffers are written by the acceptance kernel; the others
   // are staged in ws and copied
-  int32_t* ids_dev = mapped(out_ids_h);
-  int32_t* acc_dev = mapped(out_accept_h);
-  int32_t* n_dev = mapped(out_n_emitted_h);
+  // the call waits for the window, so where host pages are device-visible
+  // every host buffer is used at its own address (no copies, no queries)
+  const bool direct = host_pages_device_visible();
+  int32_t* ids_dev = mapped(out_ids_h, direct);
+  int32_t* acc_dev = mapped(out_accept_h, direct);
+  int32_t* n_dev = mapped(out_n_emitted_h, direct);
   const bool head_dev = acc_dev && n_dev;
   st = window_host_enqueue(weight, act_h, rows, hidden, vocab, path, tokens_h, parent_h, n_nodes,
                            q_ids_h, q_logits_h, hist_h, hist_len, policy, seed, position, logits,
                            pen_logits, ws, ws_bytes, s, ids_dev ? ids_dev : out + 2,
-                           head_dev ? acc_dev : out, head_dev ? n_dev : out + 1);
+                           head_dev ? acc_dev : out, head_dev ? n_dev : out + 1, direct);
   if (st != VR_OK) return st;
   // a pageable accept/n copy is the last one enqueued: the call waits once
   int32_t head[2];
@@ -570,7 +600,7 @@ int vr_verify_window_host_async(const uint16_t* weight, const float* act_h, int 
   int32_t* out = dev ? dev : at<int32_t>(ws, layout(rows, hidden, vocab).st_out);
   st = window_host_enqueue(weight, act_h, rows, hidden, vocab, path, tokens_h, parent_h, n_nodes,
                            q_ids_h, q_logits_h, hist_h, hist_len, policy, seed, position, logits,
-                           pen_logits, ws, ws_bytes, s, out + 2, out, out + 1);
+                           pen_logits, ws, ws_bytes, s, out + 2, out, out + 1, false);
   if (st != VR_OK || dev) return st;
   return cudaMemcpyAsync(out_h, out, static_cast<size_t>(2 + rows) * sizeof(int32_t),
                          cudaMemcpyDeviceToHost, s) == cudaSuccess
