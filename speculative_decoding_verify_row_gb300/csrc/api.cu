@@ -191,7 +191,7 @@ int sample_stages(const ReqTable& tab, int n_req, int rows, int vocab, float* ta
                               at<unsigned long long>(ws, L.status + kReqMaskOff),
                               at<int32_t>(ws, L.pool_ids), at<float>(ws, L.pool_vals), tab,
                               at<int4>(ws, L.dec), at<int32_t>(ws, L.status),
-                              any_active && any_q, any_active ? target : nullptr, early, s);
+                              any_active ? target : nullptr, early, s);
   int st;
   if (any_active) {
     st = launch_penalize(tab, rows, target, vocab, any_q, at<int32_t>(ws, L.status), s);

@@ -89,11 +89,17 @@ struct RowsShared {
   uint64_t pool[kPool];
   int ccount;
 
-  // the row's penalty history (built before the wait)
+  // the row's penalty history and what it implies, built before the wait:
+  // its distinct in-vocabulary tokens with their counts, and the distinct
+  // 32-row groups they fall in
   int32_t H[VR_MAX_PENALTY_WINDOW];
   int32_t par[VR_MAX_WINDOW_ROWS];
   int32_t path[VR_MAX_WINDOW_ROWS];
   int h_len, h_bad;
+  int32_t tok_u[VR_MAX_PENALTY_WINDOW];
+  int32_t cnt_u[VR_MAX_PENALTY_WINDOW];
+  int32_t grp_u[VR_MAX_PENALTY_WINDOW];
+  int n_u, n_grp;
 };
 
 struct RowShared {
@@ -598,9 +604,9 @@ __device__ void prepare_row(const ReqDev& rq, int row, bool with_q, RowShared& r
 }
 
 // The row's decisions (emit draw y, residual draw z, accept bit) once its
-// pool is known; prepare_row ran before, with q built there unless q_now.
-__device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShared& rs,
-                           int4* dec, bool live = true) {
+// pool is known; prepare_row ran before, and built q.
+__device__ void decide_row(const ReqDev& rq, int row, int n, RowShared& rs, int4* dec,
+                           bool live = true) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const vr_policy& pol = rq.pol;
   const int local = row - rq.row0;
@@ -614,11 +620,7 @@ __device__ void decide_row(const ReqDev& rq, int row, int n, bool q_now, RowShar
   }
   const bool reject_row = rs.chain && local < rq.n_nodes;
 
-  if (warp == 0) {
-    policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
-  } else if (warp == 1 && reject_row && q_now) {
-    build_q(rq, local, rs);
-  }
+  if (warp == 0) policy_warp(rs.vals, n, pol, rs.e, rs.pc, &rs.m, &rs.S);
   block_sync();
   if (warp != 0) return;
 
@@ -815,7 +817,6 @@ struct SampleArgs {
   int4* dec;               // [rows]
   int32_t* status;
   int decide;              // 0: pools only
-  int q_after_wait;        // q logits penalised in this window (built after the wait)
   float* pen_logits;       // row kernel: penalties applied in place here (== logits), or null
   int warm;                // row kernel: run the instruction warm-up pass before the wait
 };
@@ -866,7 +867,7 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
   const ReqDev& rq = rs.req;
   const int b = rs.req_b;
   if (!prepared) prepare_row(rq, row, true, rs);
-  decide_row(rq, row, n, prepared && a.q_after_wait, rs, a.dec, live);
+  decide_row(rq, row, n, rs, a.dec, live);
   if (!live) return;
 
   // Chains of at most 32 rows: no walk.  Each row writes its own output slot
@@ -1014,15 +1015,21 @@ __device__ void build_row_history(const ReqDev& rq, int local, RowsShared& sr) {
   block_sync();
 }
 
-// Penalise the CTA's row in place (each distinct token of H once), refresh
-// the group maxima the penalties touched, and write the penalised copy of
-// the draft candidates of node `local` (a chain's node is checked against
-// this row).  Runs after the wait.
-__device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vocab,
-                                 uint32_t* gmax_row, RowsShared& sr) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Everything of the row's penalties that needs no logits, before the wait:
+// the distinct in-vocabulary tokens of H with their counts (O(W^2) compares),
+// the distinct 32-row groups they touch, and, for a chain node checked
+// against this row, its draft candidates penalised with this row's history
+// (their logits are an input, and nothing reads the penalised copy before
+// this kernel builds q from it).
+__device__ void prepare_penalties(const ReqDev& rq, int local, int vocab, RowsShared& sr) {
+  const int tid = threadIdx.x;
   const vr_policy& pol = rq.pol;
   const int len = sr.h_len;
+  if (tid == 0) {
+    sr.n_u = 0;
+    sr.n_grp = 0;
+  }
+  block_sync();
   for (int j = tid; j < len; j += THREADS) {
     const int t = sr.H[j];
     bool first = true;
@@ -1033,44 +1040,19 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
         if (i < j) first = false;
       }
     }
-    if (first && t >= 0 && t < vocab) row[t] = penalize_value(__ldcg(row + t), count, pol);
+    if (first && t >= 0 && t < vocab) {
+      const int u = atomicAdd(&sr.n_u, 1);
+      sr.tok_u[u] = t;
+      sr.cnt_u[u] = count;
+    }
   }
-  __threadfence();     // the rewritten logits reach L2 before anyone reads them there
   block_sync();
-  // a warp per history slot: the first slot of each touched group refreshes
-  // that group's maximum from the penalised row.  A warp takes eight of its
-  // slots at a time and issues their loads together.
-  constexpr int NW = THREADS / 32, SB = 8;
-  for (int j0 = warp; j0 < len; j0 += NW * SB) {
-    int gs[SB];
-    float x[SB];
-#pragma unroll
-    for (int b = 0; b < SB; ++b) {
-      const int j = j0 + b * NW;       // the same for every lane of the warp
-      int g = -1;
-      if (j < len) {
-        const int t = sr.H[j];
-        if (t >= 0 && t < vocab) {
-          g = t >> 5;
-          bool seen = false;
-          for (int i = lane; i < j; i += 32) {
-            const int u = sr.H[i];
-            seen |= (u >= 0) & (u < vocab) & ((u >> 5) == g);
-          }
-          if (__any_sync(0xffffffffu, seen)) g = -1;
-        }
-      }
-      gs[b] = g;
-      const long long v = static_cast<long long>(g < 0 ? 0 : g) * 32 + lane;
-      x[b] = __ldcg(row + (v < vocab ? v : 0));     // unconditional: loads overlap
-    }
-#pragma unroll
-    for (int b = 0; b < SB; ++b) {
-      if (gs[b] < 0) continue;
-      const int v = gs[b] * 32 + lane;
-      const uint32_t m = __reduce_max_sync(0xffffffffu, v < vocab ? float_key(x[b]) : 0u);
-      if (lane == 0) gmax_row[gs[b]] = m;
-    }
+  const int n_u = sr.n_u;
+  for (int u = tid; u < n_u; u += THREADS) {
+    const int g = sr.tok_u[u] >> 5;
+    bool first = true;
+    for (int v = 0; v < u; ++v) first &= (sr.tok_u[v] >> 5) != g;
+    if (first) sr.grp_u[atomicAdd(&sr.n_grp, 1)] = g;
   }
   // the node's draft candidates, penalised with this row's history
   const bool chain_node = rq.q_ids && local < rq.n_nodes &&
@@ -1079,10 +1061,47 @@ __device__ void penalize_own_row(const ReqDev& rq, int local, float* row, int vo
     const int32_t t = rq.q_ids[static_cast<size_t>(local) * kQCand + tid];
     int count = 0;
     for (int i = 0; i < len; ++i) count += (sr.H[i] == t);
-    const float x = __ldcg(rq.q_logits_in + static_cast<size_t>(local) * kQCand + tid);
+    const float x = rq.q_logits_in[static_cast<size_t>(local) * kQCand + tid];
     rq.q_pen[static_cast<size_t>(local) * kQCand + tid] = count ? penalize_value(x, count, pol) : x;
   }
-  __threadfence();     // group maxima and q reach L2 before they are read there
+  __threadfence();     // q reaches L2 before build_q reads it there
+  block_sync();
+}
+
+// After the wait: penalise the CTA's row in place (each distinct token of H
+// once, from the list prepare_penalties built), then refresh the maxima of
+// the groups the penalties touched.  A warp takes eight groups at a time and
+// issues their loads together.
+__device__ void apply_penalties(const vr_policy& pol, float* row, int vocab, uint32_t* gmax_row,
+                                RowsShared& sr) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_u = sr.n_u, n_grp = sr.n_grp;
+  for (int u = tid; u < n_u; u += THREADS) {
+    const int t = sr.tok_u[u];
+    row[t] = penalize_value(__ldcg(row + t), sr.cnt_u[u], pol);
+  }
+  __threadfence();     // the rewritten logits reach L2 before anyone reads them there
+  block_sync();
+  constexpr int NW = THREADS / 32, SB = 8;
+  for (int g0 = warp; g0 < n_grp; g0 += NW * SB) {
+    float x[SB];
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      const int k = g0 + b * NW;       // the same for every lane of the warp
+      const long long v = static_cast<long long>(k < n_grp ? sr.grp_u[k] : 0) * 32 + lane;
+      x[b] = __ldcg(row + (v < vocab ? v : 0));     // unconditional: loads overlap
+    }
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      const int k = g0 + b * NW;
+      if (k >= n_grp) continue;
+      const int g = sr.grp_u[k];
+      const int v = g * 32 + lane;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, v < vocab ? float_key(x[b]) : 0u);
+      if (lane == 0) gmax_row[g] = m;
+    }
+  }
+  __threadfence();     // group maxima reach L2 before they are read there
   block_sync();
 }
 
@@ -1129,9 +1148,12 @@ __global__ void __launch_bounds__(THREADS, 2)
   const SampleArgs& a = s_args;
   const ReqDev& rq0 = rs.req;
   const bool pen = a.pen_logits && penalties_active(rq0.pol);
-  prepare_row(rq0, row, !a.q_after_wait, rs);
+  if (pen) {
+    build_row_history(rq0, row - rq0.row0, sr);
+    prepare_penalties(rq0, row - rq0.row0, a.vocab, sr);
+  }
+  prepare_row(rq0, row, true, rs);
   prepare_accept(rq0, a.vocab, as);
-  if (pen) build_row_history(rq0, row - rq0.row0, sr);
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
   const uint32_t* gm = gmax + static_cast<size_t>(row) * ngroups;
 
@@ -1152,8 +1174,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (live) pdl_wait();
     if (live && pen) {
       if (sr.h_bad && tid == 0) set_status(a.status, VR_DEV_BAD_PARENT);
-      penalize_own_row(rq0, row - rq0.row0, a.pen_logits + static_cast<size_t>(row) * a.vocab,
-                       a.vocab, gmax + static_cast<size_t>(row) * ngroups, sr);
+      apply_penalties(rq0.pol, a.pen_logits + static_cast<size_t>(row) * a.vocab, a.vocab,
+                      gmax + static_cast<size_t>(row) * ngroups, sr);
     }
 
     if (rq0.pol.temperature == 0.f) {
@@ -1356,7 +1378,6 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
   a.dec = dec;
   a.status = status;
   a.decide = tab ? 1 : 0;
-  a.q_after_wait = 1;
   a.pen_logits = nullptr;
   const size_t smem = sizeof(smp::StageShared);
   static std::atomic<bool> attr_set[kMaxDevices];
@@ -1376,7 +1397,7 @@ bool sample_rows_supported(int vocab) {
 int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
                        uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
                        float* pool_vals, const ReqTable& tab, int4* dec, int32_t* status,
-                       bool q_after_wait, float* pen_logits, bool warm, cudaStream_t stream) {
+                       float* pen_logits, bool warm, cudaStream_t stream) {
   smp::SampleArgs a{};
   a.logits = logits;
   a.vocab = vocab;
@@ -1388,7 +1409,6 @@ int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
   a.dec = dec;
   a.status = status;
   a.decide = 1;
-  a.q_after_wait = q_after_wait ? 1 : 0;
   a.pen_logits = pen_logits;
   a.warm = warm ? 1 : 0;
   const size_t smem = sizeof(smp::RowsShared);

@@ -107,17 +107,17 @@ int launch_sample(const float* logits, int rows, int vocab, uint64_t* cand, uint
 // the same stage for rows whose group maxima gmax [rows][ceil(vocab/32)]
 // (largest order key per 32 vocabulary rows) are known: one CTA per row
 bool sample_rows_supported(int vocab);
-// q_after_wait: some request's draft logits are penalised in this window, so
-// q is built after the wait.  warm: the kernel's CTAs start well before its
-// wait returns (they fit beside the projection), so it first runs its body
-// once without effect to load its instructions.  pen_logits (== logits, or null): the kernel
-// applies each active request's penalties to its own rows there first (and
-// refreshes gmax), so no penalty kernel runs before it.
+// warm: the kernel's CTAs start well before its wait returns (they fit beside
+// the projection), so it first runs its body once without effect to load its
+// instructions.  pen_logits (== logits, or null): the kernel applies each
+// active request's penalties to its own rows there first (and refreshes
+// gmax), so no penalty kernel runs before it; the counts, and the penalised
+// draft candidates, are prepared before its wait.
 int launch_sample_rows(const float* logits, int rows, int vocab, uint32_t* gmax,
                        uint32_t* req_ticket, unsigned long long* req_mask, int32_t* pool_ids,
                        float* pool_vals,
-                       const ReqTable& tab, int4* dec, int32_t* status, bool q_after_wait,
-                       float* pen_logits, bool warm, cudaStream_t stream);
+                       const ReqTable& tab, int4* dec, int32_t* status, float* pen_logits,
+                       bool warm, cudaStream_t stream);
 
 int launch_policy(const float* pool_vals, int rows, int pool_len, const vr_policy& pol,
                   int32_t* out_m, float* out_e, float* out_S, cudaStream_t stream);
