@@ -150,3 +150,36 @@ def test_topk_widths(k, V):
     if k == 64:
         pid, pval = gpu_pool(x)
         assert np.array_equal(pid, ids) and np.array_equal(pval.view(np.uint32), vals.view(np.uint32))
+
+
+def test_pools_and_projection_on_a_second_device():
+    """Kernel attributes (shared-memory limits) and SM counts belong to a
+    device: the select and the tensor-core projection run on cuda:1 after
+    cuda:0 and both match the oracle.  Skipped with one GPU."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two CUDA devices")
+    from speculative_decoding_verify_row_gb300 import synth
+    from gpu_common import assert_logits_close
+    V, H, R = 151936, 64, 4
+    x = adversarial_rows(R, V, 4242)
+    rng = np.random.default_rng(4243)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((5000, H)).astype(np.float32) * np.float32(0.1))
+    A = rng.standard_normal((R, H)).astype(np.float32)
+    ref = ov.project(W, A)
+    for d in (0, 1):
+        with torch.cuda.device(d):
+            dv = torch.device("cuda", d)
+            ids = torch.empty((R, 64), dtype=torch.int32, device=dv)
+            vals = torch.empty((R, 64), dtype=torch.float32, device=dv)
+            vb.verify_select(torch.from_numpy(x).to(dv), ids, vals, vb.workspace(R, 8, V, device=dv))
+            logits = torch.empty((R, 5000), dtype=torch.float32, device=dv)
+            wd = torch.from_numpy(W.view(np.int16)).to(dv)
+            vb.verify_project(wd, torch.from_numpy(A).to(dv), logits, vb.workspace(R, H, 5000, device=dv),
+                              path=vb.VR_PATH_TC)
+            torch.cuda.synchronize(dv)
+        ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+        for r in range(R):
+            ref_ids, ref_vals = ov.target_pool(x[r])
+            assert np.array_equal(ids[r], ref_ids), (d, r)
+            assert same_bits_f32(vals[r], ref_vals), (d, r)
+        assert_logits_close(logits.cpu().numpy(), ref)
