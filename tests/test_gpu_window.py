@@ -688,3 +688,39 @@ def test_largest_batched_call(path):
         n_em = int(keep[b]["n"].item())
         assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
         assert int(keep[b]["acc"].item()) == ref.accept, b
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_FFMA])
+@pytest.mark.parametrize("rows", [31, 32, 33])
+@pytest.mark.parametrize("mode", ["greedy", "sampled_q", "point_mass"])
+def test_chains_at_the_acceptance_word_limit(rows, mode, path):
+    """Chains of at most 32 rows end with one done/accept word per request,
+    longer ones with the walk over the rows' decisions: at 31, 32 and 33 rows
+    the result equals the oracle's window on the GPU's own logits, with drafts
+    that agree with the argmax for a long prefix so that the acceptance walks
+    deep."""
+    H, V = 64, 5000
+    n = rows - 1
+    rng = np.random.default_rng(3100 + rows + 7 * path)
+    W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.3))
+    A = rng.standard_normal((rows, H)).astype(np.float32)
+    L64 = ov.project(W, A)
+    am = [int(ov.target_pool(L64[r].astype(np.float32))[0][0]) for r in range(rows)]
+    stop = n - 2 if rows % 2 else n                     # a late mismatch, or none
+    tokens = np.array([am[j] if j != stop else (am[j] + 1) % V for j in range(n)], np.int32)
+    q_ids = q_log = None
+    if mode == "sampled_q":
+        q_ids = rng.integers(0, V, (n, 8)).astype(np.int32)
+        q_ids[:, 0] = tokens
+        q_log = rng.standard_normal((n, 8)).astype(np.float32) + np.float32(4.0) * (
+            np.arange(8) == 0).astype(np.float32)
+    pol = ov.Policy() if mode == "greedy" else ov.Policy(temperature=0.3, top_k=0, top_p=0.99)
+    for seed in range(3):
+        win = run_window(dev_weight(W), A, tokens, pol, seed, 777, q_ids=q_ids, q_log=q_log,
+                         path=path)
+        g_logits = win["logits"].cpu().numpy()
+        assert_logits_close(g_logits, L64)
+        ref = ov.verify_window(g_logits, tokens, None, q_ids, q_log, (), pol, seed, 777)
+        assert list(win["ids"][:win["n"]]) == ref.emitted and win["accept"] == ref.accept, seed
+        if mode == "greedy":
+            assert win["accept"] == min(stop, n)
