@@ -319,7 +319,8 @@ __device__ bool block_top64_filtered(const uint64_t (&x)[N], SelectShared& sh) {
 }
 
 // The float whose order key is k (the inverse of float_key); NaN, whose key
-// is 0 whatever its bits, is read back from the row.
+// is 0 whatever its bits, is read back from the row, so id must be a real
+// entry's (never a padding entry's).
 __device__ __forceinline__ float value_of_key(uint32_t k, const float* row, int32_t id) {
   if (k == 0u) return __ldcg(row + id);
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
@@ -850,9 +851,14 @@ __device__ void finish_row(const SampleArgs& a, const ReqTable& tab, int row, co
   if (tid < kPool) {
     int32_t id = -1;
     float v = __int_as_float(0x7fffffff);
-    if (tid < n) {
-      id = static_cast<int32_t>(packed_id(pool[tid]));
-      v = value_of_key(static_cast<uint32_t>(pool[tid] >> 32), rp, id);
+    // A zero entry is padding (its id decodes to -1).  A pool has fewer than
+    // n entries only in the row kernel's warm-up pass, whose group maxima and
+    // logits may be mid-rewrite and disagree; such an entry keeps id -1 and a
+    // NaN and never reaches the logits reload in value_of_key.
+    const uint64_t p = tid < n ? pool[tid] : 0ull;
+    if (p != 0ull) {
+      id = static_cast<int32_t>(packed_id(p));
+      v = value_of_key(static_cast<uint32_t>(p >> 32), rp, id);
     }
     if (live && tid < a.out_k) {
       a.pool_ids[static_cast<size_t>(row) * a.out_k + tid] = id;

@@ -168,6 +168,51 @@ def test_sampled_chain_full_size(big_weights_4096):
     assert stats["compared"] >= 4
 
 
+@pytest.mark.parametrize("mode", ["greedy", "sampled", "penalised"])
+def test_window_over_stale_buffers(big_weights_4096, mode):
+    """A 4-row window's row kernel starts while the projection runs and works
+    once through the logits and group maxima as they stand, before its wait.
+    Here both hold another window's values and the logits are then set to
+    -inf, so that the stale maxima pick groups with no entry at their level
+    (an empty pool in that pass).  The window must give exactly what it gives
+    on fresh buffers.  The logits sit behind a 64-float guard inside their
+    allocation."""
+    bw = big_weights_4096
+    R, V, H = 4, 151936, 4096
+    pol = {"greedy": ov.Policy(),
+           "sampled": ov.Policy(temperature=0.7, top_k=-1, min_p=0.05, top_p=0.95),
+           "penalised": ov.Policy(temperature=0.7, top_k=0, min_p=0.05, top_p=0.95, repeat=1.1,
+                                  presence=1.5, frequency=0.2, window=64)}[mode]
+    hist = synth.zipf_history(4096, V, seed=41) if mode == "penalised" else None
+    A, L64, q_ids, q_log, drafts = chain_inputs(bw, 3, 40)
+    fresh = run_window(bw.dev, A, drafts, pol, 40, 4096, q_ids=q_ids, q_log=q_log, hist=hist,
+                       separate_pen=False)
+
+    guard = torch.zeros(64 + R * V, dtype=torch.float32, device="cuda")
+    logits = guard[64:].view(R, V)
+    ws = vb.workspace(R, H, V)
+    out = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ne = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hd = None if hist is None else dev(hist)
+
+    def window(act, tokens, qi, ql):
+        vb.verify_window(bw.dev, dev(act), dev(tokens), bpol(pol), 40, 4096, logits, out, acc, ne,
+                         ws, q_ids=dev(qi), q_logits=dev(ql), hist=hd)
+
+    A2, _, q_ids2, q_log2, drafts2 = chain_inputs(bw, 3, 41)
+    window(A2, drafts2, q_ids2, q_log2)           # another window's logits and maxima
+    logits.fill_(-float("inf"))
+    window(A, drafts, q_ids, q_log)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    assert torch.equal(logits.view(torch.int32), fresh["logits"].view(torch.int32))
+    n = int(ne.item())
+    assert (n, int(acc.item())) == (fresh["n"], fresh["accept"])
+    assert list(out.cpu().numpy()[:n]) == list(fresh["ids"][:n])
+    assert torch.all(guard[:64] == 0)
+
+
 def test_penalised_chain_full_size(big_weights_4096):
     """k 8 (9 rows), 4096-token Zipf(1.1) history, W 64, repeat 1.1,
     presence 1.5, frequency 0.2, top-k 0 (the 64-wide pool).  The last
