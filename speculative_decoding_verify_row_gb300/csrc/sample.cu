@@ -46,7 +46,7 @@ constexpr int MAXR = VR_MAX_WINDOW_ROWS;
 
 struct SelectShared {
   uint32_t hist[MAX_BINS];
-  uint64_t gather[GATHER_MAX];
+  __align__(16) uint64_t gather[GATHER_MAX];
   uint64_t out[kPool];
   uint64_t sorted[kPool];
   uint64_t warp_thr[THREADS / 32];
@@ -65,7 +65,7 @@ constexpr int FAST_CAP = 256;                // entries at or above the threshol
 
 struct FastShared {
   uint32_t buf[2][THREADS];
-  uint64_t gather[FAST_CAP];
+  __align__(16) uint64_t gather[FAST_CAP];
   uint64_t sorted[kPool];
   uint32_t warp_cnt[THREADS / 32];
   uint32_t thr;
@@ -85,7 +85,7 @@ struct RowsShared {
     SelectShared sel;
     FastShared fast;
   };
-  uint64_t cands[C_MAX];
+  __align__(16) uint64_t cands[C_MAX];
   uint64_t pool[kPool];
   int ccount;
 
@@ -244,18 +244,33 @@ __device__ void block_top64(const uint64_t (&x)[N], SelectShared& sh) {
   block_sync();
 }
 
-// cand[0..n) (distinct composites, n <= THREADS) -> sorted[rank] for the
-// ranks below 64 (sorted zeroed by the caller).  Each candidate's rank is
-// counted by q = 4, 2 or 1 threads (as n allows), each over every q-th
-// candidate, and summed by shuffles.
+// cand[0..n) (distinct composites, n <= THREADS; cand 16-byte aligned) ->
+// sorted[rank] for the ranks below 64 (sorted zeroed by the caller).  Each
+// candidate's rank is counted by q = 4, 2 or 1 threads (as n allows), each
+// over every q-th pair of entries, and summed by shuffles.  Pairs are read as
+// one 16-byte load, four pairs at a time: each comparison waits on no other.
 __device__ __forceinline__ void rank_into(const uint64_t* cand, int n, uint64_t* sorted) {
   const int tid = threadIdx.x;
   const int q = n <= THREADS / 4 ? 4 : (n <= THREADS / 2 ? 2 : 1);
   const int c = tid / q, part = tid % q;
   const uint64_t me = c < n ? cand[c] : 0ull;
   int rank = 0;
-  if (c < n)
-    for (int j = part; j < n; j += q) rank += cand[j] > me ? 1 : 0;
+  if (c < n) {
+    const ulonglong2* pairs = reinterpret_cast<const ulonglong2*>(cand);
+    const int np = n >> 1;          // whole pairs; an odd n leaves cand[n - 1]
+    int k = part;
+    for (; k + 3 * q < np; k += 4 * q) {
+      const ulonglong2 p0 = pairs[k], p1 = pairs[k + q], p2 = pairs[k + 2 * q],
+                       p3 = pairs[k + 3 * q];
+      rank += (p0.x > me) + (p0.y > me) + (p1.x > me) + (p1.y > me) + (p2.x > me) +
+              (p2.y > me) + (p3.x > me) + (p3.y > me);
+    }
+    for (; k < np; k += q) {
+      const ulonglong2 p0 = pairs[k];
+      rank += (p0.x > me) + (p0.y > me);
+    }
+    if ((n & 1) && part == np % q) rank += cand[n - 1] > me ? 1 : 0;
+  }
   if (q >= 2) rank += __shfl_xor_sync(0xffffffffu, rank, 1);
   if (q >= 4) rank += __shfl_xor_sync(0xffffffffu, rank, 2);
   if (c < n && part == 0 && rank < kPool) sorted[rank] = me;
