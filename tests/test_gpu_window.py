@@ -497,8 +497,37 @@ def test_row_pools_on_crafted_logits(V, mode, path):
     vocabularies with fewer than 64 groups.
     Pools must equal the oracle's pool of the same rows bit for bit, and the
     window's result the oracle's window on them."""
+    _check_crafted_window(_crafted_rows(V, seed=V), V, mode, path)
+
+
+def _tied_group_rows(V, seed):
+    """Four rows whose top value fills whole 32-id groups: 96 groups (3072
+    tied entries), 97 groups, exactly 64 groups (2048, all the gather can
+    hold) and 64 groups plus one more top entry in a 65th.  The row kernel
+    must pick the 64 lowest-index groups among more than 64 tied maxima and
+    rank a full gather of tied candidates.  The rest are standard normal
+    draws, far below the top value 8."""
+    rng = np.random.default_rng(seed)
+    rows = rng.standard_normal((4, V)).astype(np.float32)
+    rows[0, :96 * 32] = 8.0
+    rows[1, :97 * 32] = 8.0
+    rows[2, :64 * 32] = 8.0
+    rows[3, :64 * 32] = 8.0
+    rows[3, 300 * 32 + 5] = 8.0
+    return rows
+
+
+@pytest.mark.parametrize("path", [vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH])
+@pytest.mark.parametrize("mode", ["greedy", "sampled", "penalised"])
+def test_row_pools_on_tied_top_groups(mode, path):
+    """Rows whose top value fills 64, 65, 96 or 97 whole groups: pools and the
+    window's result equal the oracle's."""
+    V = 151936
+    _check_crafted_window(_tied_group_rows(V, seed=11), V, mode, path)
+
+
+def _check_crafted_window(rows, V, mode, path):
     H, R = 64, 4
-    rows = _crafted_rows(V, seed=V)
     rng = np.random.default_rng(V + 1)
     W = synth.f32_to_bf16_bits(rng.standard_normal((V, H)).astype(np.float32) * np.float32(0.1))
     for r in range(R):
