@@ -68,6 +68,7 @@ struct FastShared {
   __align__(16) uint64_t gather[FAST_CAP];
   uint64_t sorted[kPool];
   uint32_t warp_cnt[THREADS / 32];
+  uint32_t warp_thr[THREADS / 32];
   uint32_t thr;
 };
 
@@ -277,13 +278,14 @@ __device__ __forceinline__ void rank_into(const uint64_t* cand, int n, uint64_t*
 }
 
 // Descending bitonic sort of one value per lane across a warp.
-__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+template <class U>
+__device__ __forceinline__ U warp_sort_desc(U v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const U o = __shfl_xor_sync(0xffffffffu, v, j);
       const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
       v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
     }
@@ -377,12 +379,17 @@ __device__ __forceinline__ uint32_t block_sort_desc(uint32_t v, uint32_t (&buf)[
 // iff i * THREADS < len (len = entries - t) and has id id0 + i * THREADS.
 // T = the 64th largest of the 256 per-thread largest keys: 64 threads hold a
 // key >= T, so at least 64 entries do, and the top 64 all have keys >= T.
+// With kmin < 64 only the first kmin entries of fs.sorted need to be exact:
+// T is then the smallest over the warps of each warp's ceil(kmin / 8)-th
+// largest per-thread key (one warp sort and one barrier instead of the block
+// sort), which at least kmin threads reach.
 // The entries with key >= T (usually about 70) are compacted by a block scan
 // and ranked as composites.  Returns false (after a barrier, nothing
 // written) when more than FAST_CAP entries reach T (many ties at T, or one
 // thread holding most of the top); the caller then takes the radix path.
 template <int NI>
-__device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, FastShared& fs) {
+__device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, FastShared& fs,
+                           int kmin = kPool) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the thread's largest held key, by a reduction tree (unheld keys are 0)
   uint32_t m[NI];
@@ -392,10 +399,20 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
   for (int w = 1; w < NI; w <<= 1)
 #pragma unroll
     for (int i = 0; i + w < NI; i += 2 * w) m[i] = max(m[i], m[i + w]);
-  const uint32_t T = block_sort_desc(m[0], fs.buf);
-  if (tid == kPool - 1) fs.thr = T;
-  block_sync();
-  const uint32_t thr = fs.thr;
+  uint32_t thr;
+  if (kmin >= kPool) {
+    const uint32_t T = block_sort_desc(m[0], fs.buf);
+    if (tid == kPool - 1) fs.thr = T;
+    block_sync();
+    thr = fs.thr;
+  } else {
+    const uint32_t srt = warp_sort_desc(m[0]);
+    if (lane == (kmin + 7) / 8 - 1) fs.warp_thr[warp] = srt;
+    block_sync();
+    thr = fs.warp_thr[0];
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) thr = fs.warp_thr[w] < thr ? fs.warp_thr[w] : thr;
+  }
   // held entries with key >= thr (bitwise tests: no branches)
   uint32_t cnt = 0;
 #pragma unroll
@@ -435,7 +452,7 @@ __device__ bool keys_top64(const uint32_t (&key)[NI], int len, uint32_t id0, Fas
 // Top 64 of one segment [s0, s1) of at most SEG_FAST entries in one pass
 // (keys_top64 on the row's float keys; thread t holds s0 + i * THREADS + t).
 __device__ bool segment_top64_fast(const float* __restrict__ rp, long long s0, long long s1,
-                                   FastShared& fs) {
+                                   FastShared& fs, int kmin = kPool) {
   const int tid = threadIdx.x;
   const int n_seg = static_cast<int>(s1 - s0);
   // every load is unconditional (entries past the segment read its first
@@ -449,7 +466,8 @@ __device__ bool segment_top64_fast(const float* __restrict__ rp, long long s0, l
   uint32_t key[PT];
 #pragma unroll
   for (int i = 0; i < PT; ++i) key[i] = float_key(v[i]);
-  return keys_top64(key, n_seg - tid, static_cast<uint32_t>(s0) + static_cast<uint32_t>(tid), fs);
+  return keys_top64(key, n_seg - tid, static_cast<uint32_t>(s0) + static_cast<uint32_t>(tid), fs,
+                    kmin);
 }
 
 // ---------------------------------------------------------------------------
@@ -509,6 +527,40 @@ __device__ const uint64_t* merge_lists(const uint64_t* lists, int nseg, MergeSha
     nl = pairs + (nl & 1);
   }
   return src[0];
+}
+
+// The row's top k (k <= RM_K, nseg <= RM_SEG) from the first k entries of
+// each segment's list: an entry at position j of list a ranks j plus, for
+// every other list, the number of its first k entries above it (each list
+// descends, zeros last, so that number is found by a fixed five-step binary
+// search; the searches of all lists run side by side).  Composites are
+// distinct, so the ranks are; entries of rank < k land in out[rank].  One
+// barrier instead of a merge round per halving.  Returns the pool (k
+// entries, zero-padded to 64).
+constexpr int RM_K = 16, RM_SEG = 16;
+__device__ const uint64_t* rank_merge(const uint64_t* lists, int nseg, int k, MergeShared& ms) {
+  const int tid = threadIdx.x;
+  const int a = tid / RM_K, j = tid % RM_K;                // nseg * RM_K <= THREADS
+  const bool mine = a < nseg && j < k;
+  uint64_t c = 0ull;
+  if (mine) c = __ldcg(lists + static_cast<size_t>(a) * kPool + j);
+  if (a < RM_SEG) ms.in[a][j] = mine ? c : 0ull;           // slots past k read as zero
+  if (tid < kPool) ms.out[0][tid] = 0ull;
+  block_sync();
+  if (mine && c != 0ull) {
+    int rank = j;
+#pragma unroll
+    for (int b = 0; b < RM_SEG; ++b) {
+      int lo = 0;
+#pragma unroll
+      for (int step = RM_K; step > 0; step >>= 1)
+        if (lo + step <= k && ms.in[b][lo + step - 1] > c) lo += step;
+      rank += (b < nseg && b != a) ? lo : 0;
+    }
+    if (rank < k) ms.out[0][rank] = c;
+  }
+  block_sync();
+  return ms.out[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -971,6 +1023,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   pdl_wait();
   const int seg = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
   const float* rp = a.logits + static_cast<size_t>(row) * a.vocab;
+  // a plain top-k of at most RM_K entries over at most RM_SEG segments:
+  // only each list's first k entries need to be exact, and the lists are
+  // merged by ranks
+  const bool small_k = !a.decide && a.out_k <= RM_K && a.nseg <= RM_SEG;
 
   // 1. the segment's top 64, stored in pool order: in one pass when the
   // segment fits the registers (the usual case), else sub-block by sub-block
@@ -980,7 +1036,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     const long long s1 = std::min<long long>(s0 + a.seg_len, a.vocab);
     uint64_t carry = 0ull;            // thread t < 64: entry t of the running list
     long long from = s0;
-    if (a.seg_len == SEG_FAST && segment_top64_fast(rp, s0, s1, st.fast)) {
+    if (a.seg_len == SEG_FAST && segment_top64_fast(rp, s0, s1, st.fast, small_k ? a.out_k : kPool)) {
       carry = tid < kPool ? st.fast.sorted[tid] : 0ull;
       from = s1;
       block_sync();
@@ -1017,8 +1073,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (!last) return;
   __threadfence();
   if (tid == 0) a.row_ticket[row] = 0u;
-  const uint64_t* pool =
-      merge_lists(a.cand + static_cast<size_t>(row) * a.nseg * kPool, a.nseg, st.mrg);
+  const uint64_t* lists = a.cand + static_cast<size_t>(row) * a.nseg * kPool;
+  const uint64_t* pool = small_k ? rank_merge(lists, a.nseg, a.out_k, st.mrg)
+                                 : merge_lists(lists, a.nseg, st.mrg);
   finish_row(a, tab, row, pool, rs, as, last, false);
 }
 
