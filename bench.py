@@ -384,11 +384,20 @@ def extra_workloads(torch, vb, synth, wd, dev, stream, n_steps):
     tp = _event_time(torch, stream,
                      lambda i: vb.verify_project(wd5, A, lg, ws, path=vb.VR_PATH_TC_BATCH,
                                                  stream=stream), max(5, n_steps // 50))
+    # the exact alternative: the same 256 rows through the three-plane path
+    tx = _event_time(torch, stream,
+                     lambda i: vb.verify_project(wd5, A, lg, ws, path=vb.VR_PATH_TC,
+                                                 stream=stream), max(5, n_steps // 100))
     out["batched_64x4_h5120"] = {"windows_per_s": nreq / t, "us_per_call": 1e6 * t, "rows": R,
                                  "path": "tc_batch", "projection_us": 1e6 * tp,
                                  "algorithmic_tflops": flops / tp / 1e12,
                                  "executed_tflops": 2 * flops / tp / 1e12,
-                                 "weight_gbs": V * H5 * 2 / tp / 1e9}
+                                 "weight_gbs": V * H5 * 2 / tp / 1e9,
+                                 "activations": "two exact bf16 planes: 16 significant bits of "
+                                                "each fp32 activation (a lone window on the "
+                                                "default path keeps all 24, so its logits' bits "
+                                                "differ from the batched call's)",
+                                 "exact_three_plane_projection_us": 1e6 * tx}
     del wd5
     out["topk_15x248320_k16"] = topk_workload(torch, vb, dev, stream, n_steps)
     return out
