@@ -152,6 +152,39 @@ def test_topk_widths(k, V):
         assert np.array_equal(pid, ids) and np.array_equal(pval.view(np.uint32), vals.view(np.uint32))
 
 
+def _small_k_edge_rows(V, seed):
+    """Rows for the top-k of at most 16 entries (per-segment threshold from
+    warp sorts, lists merged by ranks): all NaN but five finite values (the
+    rest of the top 16 are NaNs, lowest ids first); one 16384-id segment all
+    NaN and another all -inf among normal draws; all equal; the top 16
+    entries all in the last, partial segment; a tie block across a segment
+    boundary straddling the 16th place."""
+    rng = np.random.default_rng(seed)
+    rows = rng.standard_normal((6, V)).astype(np.float32)
+    rows[0] = np.nan
+    rows[0, rng.choice(V, 5, replace=False)] = rng.standard_normal(5).astype(np.float32)
+    if V > 2 * 16384:
+        rows[1, 16384:2 * 16384] = np.nan
+        rows[1, 2 * 16384:min(V, 3 * 16384)] = -np.inf
+    rows[2] = np.float32(0.25)
+    rows[3, V - 20:] = np.float32(9.0) + np.arange(20, dtype=np.float32) / 8
+    b = min(16384, V // 2)
+    rows[4, b - 12:b + 12] = rows[4].max() + 1
+    rows[5] = rng.choice(np.float32([1.0, 0.5, -0.0, 0.0]), V).astype(np.float32)
+    return rows
+
+
+@pytest.mark.parametrize("k", [1, 2, 7, 16])
+@pytest.mark.parametrize("V", [300, 20000, 248320, 262144])
+def test_small_k_topk_edges(k, V):
+    x = _small_k_edge_rows(V, seed=V + k)
+    ids, vals = gpu_topk(x, k)
+    for r in range(x.shape[0]):
+        ref_ids, ref_vals = ov.top_k_entries(x[r], k)
+        assert np.array_equal(ids[r], ref_ids), (r, k, V)
+        assert np.array_equal(vals[r].view(np.uint32), ref_vals.view(np.uint32)), (r, k, V)
+
+
 def test_pools_and_projection_on_a_second_device():
     """Kernel attributes (shared-memory limits) and SM counts belong to a
     device: the select and the tensor-core projection run on cuda:1 after
