@@ -1,0 +1,90 @@
+"""Seeded random windows against the oracle.  Each case draws its own shape,
+projection path and policy: 1-33 rows as a chain or a random token tree,
+vocabularies from 64 to 70001 (most not multiples of 32), hidden sizes from
+64 to 520, greedy, sampled or penalised requests, drafts with their
+re-scored candidates or as point masses.  Every window is checked stage-wise
+as the full-size window tests check theirs (logits against the fp64 oracle;
+the GPU sampler against the oracle on the same float32 logits, bit for bit;
+the fused window against the GPU's own stages; the oracle end to end when
+both sides' pools agree), so a fault that only some combination of shape,
+path and policy reaches shows up here."""
+import numpy as np
+import pytest
+
+from oracle import verify as ov
+from speculative_decoding_verify_row_gb300 import binding as vb, synth
+from gpu_common import require_gpu, dev_weight
+import test_gpu_window as tw
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [vb.VR_PATH_AUTO, vb.VR_PATH_TC, vb.VR_PATH_TC_BATCH, vb.VR_PATH_FFMA]
+VOCABS = [64, 100, 999, 4097, 12345, 32768, 70001]
+HIDDENS = [64, 128, 200, 256, 520]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _policy(rng):
+    kind = rng.choice(["greedy", "sampled", "penalised"], p=[0.3, 0.4, 0.3])
+    if kind == "greedy":
+        return ov.Policy()
+    pol = dict(temperature=float(rng.choice([0.5, 0.7, 1.3])),
+               top_k=int(rng.choice([-1, 0, 1, 5, 20, 64])),
+               min_p=float(rng.choice([0.0, 0.05, 0.2])),
+               top_p=float(rng.choice([1.0, 0.9, 0.5])))
+    if kind == "penalised":
+        pol.update(repeat=float(rng.choice([1.0, 1.1, 1.3])),
+                   presence=float(rng.choice([0.0, 0.5, 1.5])),
+                   frequency=float(rng.choice([0.0, 0.2])),
+                   window=int(rng.choice([1, 8, 64, 200])))
+    return ov.Policy(**pol)
+
+
+def _case(seed):
+    """Inputs of one random window, drawn from the case's seed."""
+    rng = np.random.default_rng(10_000 + seed)
+    V, H = int(rng.choice(VOCABS)), int(rng.choice(HIDDENS))
+    k = int(rng.integers(0, 33))
+    path = int(rng.choice(PATHS))
+    pol = _policy(rng)
+    W = synth.weights(V, H, seed=20_000 + seed)
+    A = synth.activations(k + 1, H, 30_000 + seed)
+    L64 = ov.project(W, A)
+    pools = [ov.target_pool(L64[r].astype(np.float32)) for r in range(k + 1)]
+    tree = k >= 2 and rng.random() < 0.3
+    parent = q_ids = q_log = None
+    if tree:
+        parent = np.array([int(rng.integers(-1, j)) for j in range(k)], np.int32)
+        # a node's token from the top of the row that scores it (its parent's
+        # row; the root row for children of the root), so that some agree
+        tokens = np.array([int(pools[p + 1][0][int(rng.integers(0, min(4, len(pools[p + 1][0]))))])
+                           for p in parent], np.int32)
+    elif k and pol.temperature > 0 and rng.random() < 0.6:
+        ids = np.stack([pools[r][0][:32] for r in range(k)])      # every vocabulary has >= 64 ids
+        vals = np.stack([pools[r][1][:32] for r in range(k)])
+        q_ids, q_log = synth.draft_candidates(ids, vals, seed=seed)
+        slot = synth.draft_choice(q_log, 0.7, seed=seed + 1)
+        tokens = q_ids[np.arange(k), slot].astype(np.int32)
+    else:
+        tokens = np.array([int(pools[r][0][int(rng.integers(0, min(3, len(pools[r][0]))))])
+                           for r in range(k)], np.int32)
+    hist = synth.zipf_history(int(rng.choice([0, 10, 500])), V, seed=seed) \
+        if pol.window > 0 else np.zeros(0, np.int32)
+    return dict(W=W, A=A, L64=L64, tokens=tokens, parent=parent, q_ids=q_ids, q_log=q_log,
+                hist=hist, pol=pol, seed=int(rng.integers(0, 2**63)),
+                position=int(rng.integers(0, 10**6)), path=path)
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_random_window(seed):
+    c = _case(seed)
+    win = tw.run_window(dev_weight(c["W"]), c["A"], c["tokens"], c["pol"], c["seed"],
+                        c["position"], parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"],
+                        hist=c["hist"], path=c["path"])
+    tw.check_window(win, c["L64"], c["tokens"], c["pol"], c["seed"], c["position"],
+                    parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"], hist=c["hist"])
+    assert 1 <= win["n"] <= len(c["tokens"]) + 1
