@@ -88,3 +88,100 @@ def test_random_window(seed):
     tw.check_window(win, c["L64"], c["tokens"], c["pol"], c["seed"], c["position"],
                     parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"], hist=c["hist"])
     assert 1 <= win["n"] <= len(c["tokens"]) + 1
+
+
+def _batched_case(seed):
+    """One random batched call: 1-24 requests of 1-9 rows (chains and random
+    trees), each with its own policy, seed, position, drafts and history,
+    on one random projection shape and path."""
+    rng = np.random.default_rng(50_000 + seed)
+    V, H = int(rng.choice(VOCABS)), int(rng.choice(HIDDENS))
+    path = int(rng.choice(PATHS))
+    n_req = int(rng.integers(1, 25))
+    ks = [int(rng.integers(0, 9)) for _ in range(n_req)]
+    R = sum(k + 1 for k in ks)
+    W = synth.weights(V, H, seed=60_000 + seed)
+    A = synth.activations(R, H, 70_000 + seed)
+    L64 = ov.project(W, A)
+    specs, r0 = [], 0
+    for b, k in enumerate(ks):
+        pol = _policy(rng)
+        pools = [ov.target_pool(L64[r0 + r].astype(np.float32)) for r in range(k + 1)]
+        parent = q_ids = q_log = None
+        if k >= 2 and rng.random() < 0.3:
+            parent = np.array([int(rng.integers(-1, j)) for j in range(k)], np.int32)
+            tokens = np.array([int(pools[p + 1][0][int(rng.integers(0, 4))]) for p in parent],
+                              np.int32)
+        elif k and pol.temperature > 0 and rng.random() < 0.5:
+            ids = np.stack([pools[r][0][:32] for r in range(k)])
+            vals = np.stack([pools[r][1][:32] for r in range(k)])
+            q_ids, q_log = synth.draft_candidates(ids, vals, seed=seed * 100 + b)
+            tokens = q_ids[np.arange(k), synth.draft_choice(q_log, 0.7, seed=seed * 100 + b + 1)]
+            tokens = tokens.astype(np.int32)
+        else:
+            tokens = np.array([int(pools[r][0][int(rng.integers(0, 3))]) for r in range(k)],
+                              np.int32)
+        hist = (synth.zipf_history(int(rng.choice([5, 300])), V, seed=seed * 100 + b)
+                if ov.penalties_active(pol) else None)
+        specs.append(dict(rows=list(range(r0, r0 + k + 1)), tokens=tokens, parent=parent,
+                          q_ids=q_ids, q_log=q_log, hist=hist, pol=pol,
+                          seed=int(rng.integers(0, 2**63)), position=int(rng.integers(0, 10**6))))
+        r0 += k + 1
+    return dict(W=W, A=A, L64=L64, R=R, H=H, V=V, path=path, specs=specs)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_batched_call(seed):
+    """Every request of a random batched call equals the oracle's window on
+    the GPU's own logits rows (penalised rows, pools, emitted ids and accept
+    counts bit for bit), and the logits match the fp64 oracle."""
+    import torch
+    from gpu_common import dev, assert_logits_close, same_bits_f32
+    c = _batched_case(seed)
+    R, H, V = c["R"], c["H"], c["V"]
+    reqs, keep = [], []
+    for s in c["specs"]:
+        k = len(s["tokens"])
+        t = dict(tok=dev(s["tokens"]) if k else None,
+                 par=None if s["parent"] is None else dev(s["parent"]),
+                 q=None if s["q_ids"] is None else dev(s["q_ids"]),
+                 ql=None if s["q_log"] is None else dev(s["q_log"]),
+                 h=None if s["hist"] is None else dev(s["hist"]),
+                 out=torch.full((k + 1,), -7, dtype=torch.int32, device="cuda"),
+                 acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                 n=torch.zeros(1, dtype=torch.int32, device="cuda"))
+        keep.append(t)
+        reqs.append(vb.make_request(k, t["tok"], tw.bpol(s["pol"]), s["seed"], s["position"],
+                                    t["out"], t["acc"], t["n"], parent=t["par"], q_ids=t["q"],
+                                    q_logits=t["ql"], hist=t["h"]))
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(logits)
+    ws = vb.workspace(R, H, V)
+    vb.verify_window_batched(dev_weight(c["W"]), dev(c["A"]), reqs, logits, ws, pen_logits=pen,
+                             path=c["path"])
+    ids = torch.empty((R, 64), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, 64), dtype=torch.float32, device="cuda")
+    vb.window_pools(ws, R, H, V, ids, vals)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    g_logits = logits.cpu().numpy()
+    assert_logits_close(g_logits, c["L64"])
+    ids, vals, g_pen = ids.cpu().numpy(), vals.cpu().numpy(), pen.cpu().numpy()
+    refs = ov.verify_batched(g_logits, [dict(tokens=s["tokens"], parent=s["parent"],
+                                             q_ids=s["q_ids"], q_logits=s["q_log"],
+                                             hist=() if s["hist"] is None else s["hist"],
+                                             pol=s["pol"], seed=s["seed"],
+                                             position=s["position"]) for s in c["specs"]])
+    for b, (s, ref) in enumerate(zip(c["specs"], refs)):
+        active = ov.penalties_active(s["pol"])
+        rows = g_pen[s["rows"]] if active else g_logits[s["rows"]]
+        if active:
+            assert same_bits_f32(rows, ref.pen_logits), b
+        for i, r in enumerate(s["rows"]):
+            want_ids, want_vals = ov.target_pool(rows[i])
+            n = 1 if s["pol"].temperature == 0.0 else len(want_ids)
+            assert np.array_equal(ids[r, :n], want_ids[:n]), (b, i)
+            assert same_bits_f32(vals[r, :n], want_vals[:n]), (b, i)
+        n_em = int(keep[b]["n"].item())
+        assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
+        assert int(keep[b]["acc"].item()) == ref.accept, b
