@@ -185,3 +185,36 @@ def test_random_batched_call(seed):
         n_em = int(keep[b]["n"].item())
         assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
         assert int(keep[b]["acc"].item()) == ref.accept, b
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("seed", range(0, 200, 10))
+def test_random_host_window(seed, pinned):
+    """The host-buffer entry point on a random window (the shapes of
+    test_random_window): pinned inputs read by the staging kernel, or pageable
+    ones copied, give the device entry point's result and logits bit for
+    bit."""
+    import torch
+    c = _case(seed)
+    wd = dev_weight(c["W"])
+    win = tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
+                        parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"], hist=c["hist"],
+                        path=c["path"], separate_pen=False)
+    if pinned:
+        host = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    else:
+        host = lambda x: torch.from_numpy(np.ascontiguousarray(x).copy())
+    opt = lambda x: None if x is None or len(x) == 0 else host(x)
+    R, H = c["A"].shape
+    V = c["W"].shape[0]
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    out = host(np.full(R, -7, np.int32))
+    ws = vb.workspace(R, H, V)
+    acc, n = vb.verify_window_host(wd, host(c["A"]), opt(c["tokens"]), tw.bpol(c["pol"]),
+                                   c["seed"], c["position"], logits, out, ws,
+                                   parent_h=opt(c["parent"]), q_ids_h=opt(c["q_ids"]),
+                                   q_logits_h=opt(c["q_log"]), hist_h=opt(c["hist"]),
+                                   path=c["path"])
+    assert (acc, n) == (win["accept"], win["n"])
+    assert list(out.numpy()[:n]) == list(win["ids"][:n])
+    assert torch.equal(logits.view(torch.int32), win["logits"].view(torch.int32))
