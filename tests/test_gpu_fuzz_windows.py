@@ -218,3 +218,40 @@ def test_random_host_window(seed, pinned):
     assert (acc, n) == (win["accept"], win["n"])
     assert list(out.numpy()[:n]) == list(win["ids"][:n])
     assert torch.equal(logits.view(torch.int32), win["logits"].view(torch.int32))
+
+
+def test_random_windows_share_one_workspace():
+    """Thirty random windows of different shapes and paths run one after
+    another through one workspace sized for the largest (as a server keeps
+    one): each gives what it gives on a fresh workspace, so no call depends
+    on what an earlier call of another shape left behind (the control region
+    is left zeroed, and every other region is written before it is read)."""
+    import torch
+    from gpu_common import dev
+    cases = [_case(seed) for seed in range(300, 330)]
+    Rm = max(c["A"].shape[0] for c in cases)
+    Hm = max(c["A"].shape[1] for c in cases)
+    Vm = max(c["W"].shape[0] for c in cases)
+    shared = vb.workspace(Rm, Hm, Vm)
+    for i, c in enumerate(cases):
+        wd = dev_weight(c["W"])
+        fresh = tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
+                              parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"],
+                              hist=c["hist"], path=c["path"], separate_pen=False)
+        R, H = c["A"].shape
+        V = c["W"].shape[0]
+        logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+        out = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+        acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ne = torch.zeros(1, dtype=torch.int32, device="cuda")
+        opt = lambda x: None if x is None or len(x) == 0 else dev(x)
+        vb.verify_window(wd, dev(c["A"]), opt(c["tokens"]), tw.bpol(c["pol"]), c["seed"],
+                         c["position"], logits, out, acc, ne, shared, parent=opt(c["parent"]),
+                         q_ids=opt(c["q_ids"]), q_logits=opt(c["q_log"]), hist=opt(c["hist"]),
+                         path=c["path"])
+        torch.cuda.synchronize()
+        assert vb.device_status(shared) == 0, i
+        n = int(ne.item())
+        assert (n, int(acc.item())) == (fresh["n"], fresh["accept"]), i
+        assert list(out.cpu().numpy()[:n]) == list(fresh["ids"][:n]), i
+        assert torch.equal(logits.view(torch.int32), fresh["logits"].view(torch.int32)), i
