@@ -255,3 +255,43 @@ def test_random_windows_share_one_workspace():
         assert (n, int(acc.item())) == (fresh["n"], fresh["accept"]), i
         assert list(out.cpu().numpy()[:n]) == list(fresh["ids"][:n]), i
         assert torch.equal(logits.view(torch.int32), fresh["logits"].view(torch.int32)), i
+
+
+def test_random_windows_on_concurrent_streams():
+    """Pairs of random windows enqueued on two streams at once, each with its
+    own buffers and workspace, give what they give alone: the library keeps
+    no state between calls outside the workspace it is handed."""
+    import torch
+    from gpu_common import dev
+    opt = lambda x: None if x is None or len(x) == 0 else dev(x)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for p in range(8):
+        cs = [_case(400 + 2 * p), _case(401 + 2 * p)]
+        alone, bufs = [], []
+        for c in cs:
+            wd = dev_weight(c["W"])
+            alone.append(tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
+                                       parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"],
+                                       hist=c["hist"], path=c["path"], separate_pen=False))
+            R, H = c["A"].shape
+            V = c["W"].shape[0]
+            bufs.append(dict(wd=wd, a=dev(c["A"]), tok=opt(c["tokens"]), par=opt(c["parent"]),
+                             q=opt(c["q_ids"]), ql=opt(c["q_log"]), h=opt(c["hist"]),
+                             lg=torch.empty((R, V), dtype=torch.float32, device="cuda"),
+                             out=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                             acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                             n=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                             ws=vb.workspace(R, H, V)))
+        torch.cuda.synchronize()
+        for c, b, s in zip(cs, bufs, streams):
+            vb.verify_window(b["wd"], b["a"], b["tok"], tw.bpol(c["pol"]), c["seed"], c["position"],
+                             b["lg"], b["out"], b["acc"], b["n"], b["ws"], parent=b["par"],
+                             q_ids=b["q"], q_logits=b["ql"], hist=b["h"], path=c["path"],
+                             stream=s)
+        torch.cuda.synchronize()
+        for i, (b, w) in enumerate(zip(bufs, alone)):
+            n = int(b["n"].item())
+            assert vb.device_status(b["ws"]) == 0, (p, i)
+            assert (n, int(b["acc"].item())) == (w["n"], w["accept"]), (p, i)
+            assert list(b["out"].cpu().numpy()[:n]) == list(w["ids"][:n]), (p, i)
+            assert torch.equal(b["lg"].view(torch.int32), w["logits"].view(torch.int32)), (p, i)
