@@ -283,7 +283,8 @@ VR_API int vr_verify_sample_accept(const float* pen_logits, int rows, int vocab,
 
 /*
  * The whole window in one call: projection -> penalties -> pool -> policy ->
- * acceptance, enqueued on `stream` with no host synchronisation.
+ * acceptance, enqueued on `stream` with no host synchronisation (kernels
+ * only, so the call may be captured into a CUDA graph and replayed).
  * logits receives the raw projection.  If the policy has active penalties:
  * pen_logits (if non-NULL) receives the penalised rows and logits stays raw;
  * if pen_logits is NULL, logits is penalised in place.  q_logits is read
@@ -301,8 +302,11 @@ VR_API int vr_verify_window(const uint16_t* weight, const float* act, int rows, 
  * (request b owns n_nodes_b + 1 consecutive rows, in the order of `reqs`)
  * and share one projection; penalties, pools, policies and acceptance run
  * per request with that request's policy, seed, position and history.
- * `reqs` is a HOST array of n_req descriptors (copied into ws before the call
- * returns).  total rows <= VR_MAX_ROWS, n_req <= VR_MAX_REQUESTS.
+ * `reqs` is a HOST array of n_req descriptors; the call copies them into the
+ * parameters of the kernels it enqueues (which store them into ws), so the
+ * array may be reused or freed as soon as the call returns, and the call may
+ * be captured into a CUDA graph (each replay uses the descriptors as they
+ * were at capture).  total rows <= VR_MAX_ROWS, n_req <= VR_MAX_REQUESTS.
  * logits/pen_logits as in vr_verify_window.
  */
 VR_API int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidden, int vocab,

@@ -392,7 +392,6 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   std::vector<ReqDev> table(n_req);
-  std::vector<int32_t> row_req(rows);
   int row0 = 0;
   for (int b = 0; b < n_req; ++b) {
     const vr_request& r = reqs[b];
@@ -401,14 +400,14 @@ int vr_verify_window_batched(const uint16_t* weight, const float* act, int hidde
     table[b] = make_req(row0, r.n_nodes, r.tokens, r.parent, r.q_ids, r.q_logits, q_pen, r.hist,
                         r.hist_len, r.policy, r.seed, r.position, r.out_ids, r.out_accept,
                         r.out_n_emitted);
-    for (int i = 0; i <= r.n_nodes; ++i) row_req[row0 + i] = b;
     row0 += r.n_nodes + 1;
   }
-  if (cudaMemcpyAsync(at<void>(ws, L.reqs), table.data(), table.size() * sizeof(ReqDev),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(at<void>(ws, L.row_req), row_req.data(), row_req.size() * sizeof(int32_t),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return VR_ERR_CUDA;
+  // staged by kernels that carry the table in their parameters (copied at
+  // launch or capture): no operation on the stream reads this call's host
+  // memory, so the call can be captured into a graph and replayed
+  if ((st = launch_stage_requests(table.data(), n_req, at<ReqDev>(ws, L.reqs),
+                                  at<int32_t>(ws, L.row_req), s)) != VR_OK)
+    return st;
 
   uint32_t* gmax = records_gmax(path, vocab) ? at<uint32_t>(ws, L.gmax) : nullptr;
   // penalties into a separate buffer: the projection writes both copies

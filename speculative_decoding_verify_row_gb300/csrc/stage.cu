@@ -61,6 +61,39 @@ __global__ void __launch_bounds__(kStageThreads)
   }
 }
 
+// The request table of a batched window, passed by value and stored into
+// the workspace with the row-to-request map, one CTA per chunk of requests.
+// Kernel parameters are copied when the launch is made (or captured into a
+// graph), so the table needs no host buffer that outlives the call; a copy
+// from the call's own host memory would, in a captured graph, read that
+// memory again at every replay, long after the call returned.
+constexpr int kReqChunk = 128;           // 128 x 136 B of requests: within the parameter space
+
+struct ReqChunk {
+  ReqDev r[kReqChunk];
+  int n;                                 // requests in this chunk
+  int b0;                                // index of its first request
+};
+
+__global__ void __launch_bounds__(kStageThreads)
+    stage_requests_kernel(const __grid_constant__ ReqChunk c, ReqDev* __restrict__ table,
+                          int32_t* __restrict__ row_req) {
+  // as for the inputs: the projection after this kernel reads only weights
+  // before its wait, and the row kernel launches only after that wait
+  pdl_trigger();
+  // the table and the map may still be read by the previous window's kernels
+  pdl_wait();
+  constexpr int W = static_cast<int>(sizeof(ReqDev) / 4);
+  static_assert(sizeof(ReqDev) % 4 == 0, "request copy");
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(c.r);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(table + c.b0);
+  for (int w = threadIdx.x; w < c.n * W; w += kStageThreads) dst[w] = src[w];
+  for (int i = threadIdx.x >> 5; i < c.n; i += kStageThreads / 32) {
+    const ReqDev& q = c.r[i];
+    for (int j = threadIdx.x & 31; j <= q.n_nodes; j += 32) row_req[q.row0 + j] = c.b0 + i;
+  }
+}
+
 }  // namespace
 
 int launch_stage_inputs(const StageSeg* segs, int nseg, cudaStream_t stream) {
@@ -84,6 +117,21 @@ int launch_stage_inputs(const StageSeg* segs, int nseg, cudaStream_t stream) {
                  cudaSuccess
              ? VR_OK
              : VR_ERR_CUDA;
+}
+
+int launch_stage_requests(const ReqDev* reqs, int n_req, ReqDev* table, int32_t* row_req,
+                          cudaStream_t stream) {
+  static_assert(sizeof(ReqChunk) <= 32000, "kernel parameter space");
+  for (int b0 = 0; b0 < n_req; b0 += kReqChunk) {
+    ReqChunk c;
+    c.n = n_req - b0 < kReqChunk ? n_req - b0 : kReqChunk;
+    c.b0 = b0;
+    for (int i = 0; i < c.n; ++i) c.r[i] = reqs[b0 + i];
+    if (launch_pdl(stage_requests_kernel, dim3(1), dim3(kStageThreads), 0, stream, c, table,
+                   row_req) != cudaSuccess)
+      return VR_ERR_CUDA;
+  }
+  return VR_OK;
 }
 
 }  // namespace vr

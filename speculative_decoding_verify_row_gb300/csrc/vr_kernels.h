@@ -57,6 +57,11 @@ struct StageSeg {
   uint32_t words;
 };
 int launch_stage_inputs(const StageSeg* segs, int nseg, cudaStream_t stream);
+// The request table of a batched window into the workspace (table[n_req],
+// row_req[rows]) by kernels that carry it in their parameters, 128 requests
+// per launch: nothing on the stream reads host memory of the call.
+int launch_stage_requests(const ReqDev* reqs, int n_req, ReqDev* table, int32_t* row_req,
+                          cudaStream_t stream);
 
 // projection
 bool encode_bf16_tile(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

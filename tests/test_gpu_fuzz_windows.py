@@ -295,3 +295,103 @@ def test_random_windows_on_concurrent_streams():
             assert (n, int(b["acc"].item())) == (w["n"], w["accept"]), (p, i)
             assert list(b["out"].cpu().numpy()[:n]) == list(w["ids"][:n]), (p, i)
             assert torch.equal(b["lg"].view(torch.int32), w["logits"].view(torch.int32)), (p, i)
+
+
+def test_random_windows_captured_in_a_cuda_graph():
+    """Six random windows captured into one CUDA graph (each with its own
+    buffers and workspace) and replayed twice give their eager results: a
+    window enqueues kernels only (no host work, no copy), so it can be
+    captured."""
+    import torch
+    from gpu_common import dev
+    opt = lambda x: None if x is None or len(x) == 0 else dev(x)
+    cases = [_case(s) for s in range(500, 506)]
+    eager, bufs = [], []
+    for c in cases:
+        wd = dev_weight(c["W"])
+        eager.append(tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
+                                   parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"],
+                                   hist=c["hist"], path=c["path"], separate_pen=False))
+        R, H = c["A"].shape
+        V = c["W"].shape[0]
+        bufs.append(dict(wd=wd, a=dev(c["A"]), tok=opt(c["tokens"]), par=opt(c["parent"]),
+                         q=opt(c["q_ids"]), ql=opt(c["q_log"]), h=opt(c["hist"]),
+                         lg=torch.empty((R, V), dtype=torch.float32, device="cuda"),
+                         out=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                         acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                         n=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                         ws=vb.workspace(R, H, V)))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c, b in zip(cases, bufs):
+            vb.verify_window(b["wd"], b["a"], b["tok"], tw.bpol(c["pol"]), c["seed"],
+                             c["position"], b["lg"], b["out"], b["acc"], b["n"], b["ws"],
+                             parent=b["par"], q_ids=b["q"], q_logits=b["ql"], hist=b["h"],
+                             path=c["path"])
+    for rep in range(2):
+        for b in bufs:
+            b["out"].fill_(-7)
+            b["lg"].fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (b, w) in enumerate(zip(bufs, eager)):
+            n = int(b["n"].item())
+            assert vb.device_status(b["ws"]) == 0, (rep, i)
+            assert (n, int(b["acc"].item())) == (w["n"], w["accept"]), (rep, i)
+            assert list(b["out"].cpu().numpy()[:n]) == list(w["ids"][:n]), (rep, i)
+            assert torch.equal(b["lg"].view(torch.int32), w["logits"].view(torch.int32)), (rep, i)
+
+
+def test_random_batched_call_captured_in_a_cuda_graph():
+    """A random batched call captured into a CUDA graph and replayed gives its
+    eager result (the request table is captured with the call)."""
+    import torch
+    from gpu_common import dev
+    c = _batched_case(7)
+    R, H, V = c["R"], c["H"], c["V"]
+    wd, a = dev_weight(c["W"]), dev(c["A"])
+
+    def requests():
+        reqs, keep = [], []
+        for s in c["specs"]:
+            k = len(s["tokens"])
+            t = dict(tok=dev(s["tokens"]) if k else None,
+                     par=None if s["parent"] is None else dev(s["parent"]),
+                     q=None if s["q_ids"] is None else dev(s["q_ids"]),
+                     ql=None if s["q_log"] is None else dev(s["q_log"]),
+                     h=None if s["hist"] is None else dev(s["hist"]),
+                     out=torch.full((k + 1,), -7, dtype=torch.int32, device="cuda"),
+                     acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                     n=torch.zeros(1, dtype=torch.int32, device="cuda"))
+            keep.append(t)
+            reqs.append(vb.make_request(k, t["tok"], tw.bpol(s["pol"]), s["seed"], s["position"],
+                                        t["out"], t["acc"], t["n"], parent=t["par"], q_ids=t["q"],
+                                        q_logits=t["ql"], hist=t["h"]))
+        return reqs, keep
+
+    def outputs(keep):
+        return [(int(t["n"].item()), int(t["acc"].item()),
+                 list(t["out"].cpu().numpy()[:int(t["n"].item())])) for t in keep]
+
+    lg = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    ws = vb.workspace(R, H, V)
+    reqs, keep = requests()
+    vb.verify_window_batched(wd, a, reqs, lg, ws, path=c["path"])
+    torch.cuda.synchronize()
+    want, want_lg = outputs(keep), lg.clone()
+    reqs2, keep2 = requests()
+    lg2 = torch.empty_like(lg)
+    ws2 = vb.workspace(R, H, V)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        vb.verify_window_batched(wd, a, reqs2, lg2, ws2, path=c["path"])
+    for rep in range(2):
+        for t in keep2:
+            t["out"].fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert vb.device_status(ws2) == 0
+        assert outputs(keep2) == want, rep
+        assert torch.equal(lg2.view(torch.int32), want_lg.view(torch.int32)), rep
