@@ -395,3 +395,45 @@ def test_random_batched_call_captured_in_a_cuda_graph():
         assert vb.device_status(ws2) == 0
         assert outputs(keep2) == want, rep
         assert torch.equal(lg2.view(torch.int32), want_lg.view(torch.int32)), rep
+
+
+def test_random_async_host_windows_captured_in_a_cuda_graph():
+    """Four random windows through the pipelined host-buffer entry point
+    (pinned inputs and [accept, n, ids] outputs) captured into a CUDA graph:
+    each replay reads the pinned inputs and writes the pinned outputs, which
+    equal the device entry point's results."""
+    import torch
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    opt = lambda x: None if x is None or len(x) == 0 else pin(x)
+    cases = [_case(s) for s in range(600, 604)]
+    want, bufs = [], []
+    for c in cases:
+        wd = dev_weight(c["W"])
+        w = tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
+                          parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"], hist=c["hist"],
+                          path=c["path"], separate_pen=False)
+        want.append((w["accept"], w["n"], list(w["ids"][:w["n"]])))
+        R, H = c["A"].shape
+        V = c["W"].shape[0]
+        bufs.append(dict(wd=wd, a=pin(c["A"]), tok=opt(c["tokens"]), par=opt(c["parent"]),
+                         q=opt(c["q_ids"]), ql=opt(c["q_log"]), h=opt(c["hist"]),
+                         lg=torch.empty((R, V), dtype=torch.float32, device="cuda"),
+                         out=torch.full((R + 2,), -7, dtype=torch.int32).pin_memory(),
+                         ws=vb.workspace(R, H, V)))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c, b in zip(cases, bufs):
+            vb.verify_window_host_async(b["wd"], b["a"], b["tok"], tw.bpol(c["pol"]), c["seed"],
+                                        c["position"], b["lg"], b["out"], b["ws"],
+                                        parent_h=b["par"], q_ids_h=b["q"], q_logits_h=b["ql"],
+                                        hist_h=b["h"], path=c["path"])
+    for rep in range(2):
+        for b in bufs:
+            b["out"].fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (b, w) in enumerate(zip(bufs, want)):
+            o = b["out"].numpy()
+            acc, n = int(o[0]), int(o[1])
+            assert (acc, n, list(o[2:2 + n])) == w, (rep, i)
