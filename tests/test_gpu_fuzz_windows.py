@@ -437,3 +437,54 @@ def test_random_async_host_windows_captured_in_a_cuda_graph():
             o = b["out"].numpy()
             acc, n = int(o[0]), int(o[1])
             assert (acc, n, list(o[2:2 + n])) == w, (rep, i)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("what", ["token", "parent", "qid"])
+def test_fused_window_flags_invalid_device_data(path, what):
+    """Device data the host cannot check (a draft token past the vocabulary,
+    a parent array that is not topological, a candidate id past the
+    vocabulary) makes the fused window emit nothing and set the status word,
+    on every path and with penalties active (the history walk meets the bad
+    parent first); the next good window on the same workspace is unaffected."""
+    import torch
+    from gpu_common import dev
+    V, H, k = 5000, 64, 3
+    W = synth.weights(V, H, seed=77)
+    A = synth.activations(k + 1, H, 78)
+    wd = dev_weight(W)
+    pol = ov.Policy(temperature=0.8, top_k=20, presence=0.5, window=16)
+    tokens = np.array([5, 6, 7], np.int32)
+    parent = q_ids = q_log = None
+    if what == "token":
+        tokens[1] = V + 3
+    elif what == "parent":
+        parent = np.array([-1, 2, 1], np.int32)          # node 1 names a later node
+    else:
+        q_ids = np.tile(np.arange(8, dtype=np.int32), (k, 1))
+        q_ids[0, 0] = tokens[0]
+        q_ids[2, 5] = V + 100
+        q_log = np.zeros((k, 8), np.float32)
+    hist = np.arange(20, dtype=np.int32)
+    ws = vb.workspace(k + 1, H, V)
+    lg = torch.empty((k + 1, V), dtype=torch.float32, device="cuda")
+    out = torch.full((k + 1,), -7, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ne = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    opt = lambda x: None if x is None else dev(x)
+    vb.verify_window(wd, dev(A), dev(tokens), tw.bpol(pol), 1, 2, lg, out, acc, ne, ws,
+                     parent=opt(parent), q_ids=opt(q_ids), q_logits=opt(q_log), hist=dev(hist),
+                     path=path)
+    torch.cuda.synchronize()
+    st = vb.device_status(ws)
+    flag = {"token": vb.VR_DEV_BAD_TOKEN, "parent": vb.VR_DEV_BAD_PARENT,
+            "qid": vb.VR_DEV_BAD_QID}[what]
+    assert st & flag, st
+    assert int(ne.item()) == 0 and int(acc.item()) == 0
+    # the status word was read and cleared: a good window runs clean
+    good = np.array([5, 6, 7], np.int32)
+    vb.verify_window(wd, dev(A), dev(good), tw.bpol(pol), 1, 2, lg, out, acc, ne, ws,
+                     hist=dev(hist), path=path)
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) == 0
+    assert 1 <= int(ne.item()) <= k + 1
