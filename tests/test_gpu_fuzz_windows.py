@@ -488,3 +488,57 @@ def test_fused_window_flags_invalid_device_data(path, what):
     torch.cuda.synchronize()
     assert vb.device_status(ws) == 0
     assert 1 <= int(ne.item()) <= k + 1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_batched_call_isolates_a_request_with_invalid_data(seed):
+    """One request of a random batched call carries a draft token past the
+    vocabulary: that request emits nothing and the status word is set, while
+    every other request still equals the oracle's window on the GPU's own
+    logits."""
+    import torch
+    from gpu_common import dev, same_bits_f32
+    c = _batched_case(100 + seed)
+    specs = c["specs"]
+    bad = next((b for b, s in enumerate(specs) if len(s["tokens"])), None)
+    if bad is None:
+        pytest.skip("no request with drafts in this draw")
+    R, H, V = c["R"], c["H"], c["V"]
+    reqs, keep = [], []
+    for b, s in enumerate(specs):
+        k = len(s["tokens"])
+        tokens = s["tokens"].copy()
+        if b == bad:
+            tokens[k - 1] = V + 7
+        t = dict(tok=dev(tokens) if k else None,
+                 par=None if s["parent"] is None else dev(s["parent"]),
+                 q=None if s["q_ids"] is None else dev(s["q_ids"]),
+                 ql=None if s["q_log"] is None else dev(s["q_log"]),
+                 h=None if s["hist"] is None else dev(s["hist"]),
+                 out=torch.full((k + 1,), -7, dtype=torch.int32, device="cuda"),
+                 acc=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                 n=torch.full((1,), -1, dtype=torch.int32, device="cuda"))
+        keep.append(t)
+        reqs.append(vb.make_request(k, t["tok"], tw.bpol(s["pol"]), s["seed"], s["position"],
+                                    t["out"], t["acc"], t["n"], parent=t["par"], q_ids=t["q"],
+                                    q_logits=t["ql"], hist=t["h"]))
+    lg = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    pen = torch.empty_like(lg)
+    ws = vb.workspace(R, H, V)
+    vb.verify_window_batched(dev_weight(c["W"]), dev(c["A"]), reqs, lg, ws, pen_logits=pen,
+                             path=c["path"])
+    torch.cuda.synchronize()
+    assert vb.device_status(ws) & vb.VR_DEV_BAD_TOKEN
+    g_logits = lg.cpu().numpy()
+    refs = ov.verify_batched(g_logits, [dict(tokens=s["tokens"], parent=s["parent"],
+                                             q_ids=s["q_ids"], q_logits=s["q_log"],
+                                             hist=() if s["hist"] is None else s["hist"],
+                                             pol=s["pol"], seed=s["seed"],
+                                             position=s["position"]) for s in specs])
+    for b, ref in enumerate(refs):
+        n_em = int(keep[b]["n"].item())
+        if b == bad:
+            assert n_em == 0 and int(keep[b]["acc"].item()) == 0
+            continue
+        assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
+        assert int(keep[b]["acc"].item()) == ref.accept, b
