@@ -96,6 +96,24 @@ def test_matches_the_workspace_select_and_the_oracle_on_two_calls_in_a_row(lib, 
         _assert_oracle_pools(x, got_ids, got_vals)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_in_sequence_match_the_oracle(lib, seed):
+    """Random row counts (up to the limit) and vocabularies (1 to 300000,
+    across the one-pass and sub-block segment sizes), one call after another
+    on the library's fixed array: every pool equals the oracle's."""
+    from speculative_decoding_verify_row_gb300 import binding as vb
+    rng = np.random.default_rng(9_000 + seed)
+    for _ in range(3):
+        R = int(rng.integers(1, vb.VR_NOALLOC_SELECT_MAX_ROWS + 1))
+        V = int(rng.choice([1, 7, 63, 64, 65, 1000, 16384, 16385, 100_003, 300_000]))
+        if R * V > 4_000_000:
+            R = max(1, 4_000_000 // V)
+        x = _rows(int(rng.integers(0, 2**31)), R, V)
+        got_ids, got_vals = _select_noalloc(lib, torch.from_numpy(x).cuda())
+        torch.cuda.synchronize()
+        _assert_oracle_pools(x, got_ids, got_vals)
+
+
 def test_later_calls_leave_free_device_memory_unchanged(lib):
     # inputs and outputs first, then one call (the first call on a device
     # loads the library's fixed array), then two more calls of different
