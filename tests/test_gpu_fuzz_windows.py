@@ -10,10 +10,11 @@ both sides' pools agree), so a fault that only some combination of shape,
 path and policy reaches shows up here."""
 import numpy as np
 import pytest
+import torch
 
 from oracle import verify as ov
 from speculative_decoding_verify_row_gb300 import binding as vb, synth
-from gpu_common import require_gpu, dev_weight
+from gpu_common import require_gpu, dev, dev_weight, assert_logits_close, same_bits_f32
 import test_gpu_window as tw
 
 pytestmark = pytest.mark.gpu
@@ -135,8 +136,6 @@ def test_random_batched_call(seed):
     """Every request of a random batched call equals the oracle's window on
     the GPU's own logits rows (penalised rows, pools, emitted ids and accept
     counts bit for bit), and the logits match the fp64 oracle."""
-    import torch
-    from gpu_common import dev, assert_logits_close, same_bits_f32
     c = _batched_case(seed)
     R, H, V = c["R"], c["H"], c["V"]
     reqs, keep = [], []
@@ -194,7 +193,6 @@ def test_random_host_window(seed, pinned):
     test_random_window): pinned inputs read by the staging kernel, or pageable
     ones copied, give the device entry point's result and logits bit for
     bit."""
-    import torch
     c = _case(seed)
     wd = dev_weight(c["W"])
     win = tw.run_window(wd, c["A"], c["tokens"], c["pol"], c["seed"], c["position"],
@@ -226,8 +224,6 @@ def test_random_windows_share_one_workspace():
     one): each gives what it gives on a fresh workspace, so no call depends
     on what an earlier call of another shape left behind (the control region
     is left zeroed, and every other region is written before it is read)."""
-    import torch
-    from gpu_common import dev
     cases = [_case(seed) for seed in range(300, 330)]
     Rm = max(c["A"].shape[0] for c in cases)
     Hm = max(c["A"].shape[1] for c in cases)
@@ -261,8 +257,6 @@ def test_random_windows_on_concurrent_streams():
     """Pairs of random windows enqueued on two streams at once, each with its
     own buffers and workspace, give what they give alone: the library keeps
     no state between calls outside the workspace it is handed."""
-    import torch
-    from gpu_common import dev
     opt = lambda x: None if x is None or len(x) == 0 else dev(x)
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     for p in range(8):
@@ -302,8 +296,6 @@ def test_random_windows_captured_in_a_cuda_graph():
     buffers and workspace) and replayed twice give their eager results: a
     window enqueues kernels only (no host work, no copy), so it can be
     captured."""
-    import torch
-    from gpu_common import dev
     opt = lambda x: None if x is None or len(x) == 0 else dev(x)
     cases = [_case(s) for s in range(500, 506)]
     eager, bufs = [], []
@@ -346,8 +338,6 @@ def test_random_windows_captured_in_a_cuda_graph():
 def test_random_batched_call_captured_in_a_cuda_graph():
     """A random batched call captured into a CUDA graph and replayed gives its
     eager result (the request table is captured with the call)."""
-    import torch
-    from gpu_common import dev
     c = _batched_case(7)
     R, H, V = c["R"], c["H"], c["V"]
     wd, a = dev_weight(c["W"]), dev(c["A"])
@@ -402,7 +392,6 @@ def test_random_async_host_windows_captured_in_a_cuda_graph():
     (pinned inputs and [accept, n, ids] outputs) captured into a CUDA graph:
     each replay reads the pinned inputs and writes the pinned outputs, which
     equal the device entry point's results."""
-    import torch
     pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
     opt = lambda x: None if x is None or len(x) == 0 else pin(x)
     cases = [_case(s) for s in range(600, 604)]
@@ -447,8 +436,6 @@ def test_fused_window_flags_invalid_device_data(path, what):
     vocabulary) makes the fused window emit nothing and set the status word,
     on every path and with penalties active (the history walk meets the bad
     parent first); the next good window on the same workspace is unaffected."""
-    import torch
-    from gpu_common import dev
     V, H, k = 5000, 64, 3
     W = synth.weights(V, H, seed=77)
     A = synth.activations(k + 1, H, 78)
@@ -496,8 +483,6 @@ def test_batched_call_isolates_a_request_with_invalid_data(seed):
     vocabulary: that request emits nothing and the status word is set, while
     every other request still equals the oracle's window on the GPU's own
     logits."""
-    import torch
-    from gpu_common import dev, same_bits_f32
     c = _batched_case(100 + seed)
     specs = c["specs"]
     bad = next((b for b, s in enumerate(specs) if len(s["tokens"])), None)
