@@ -58,6 +58,23 @@ def test_pool_matches_oracle(V, kind):
         assert np.all(ids[r, n:] == -1)
 
 
+@pytest.mark.parametrize("V", [1_500_007, 4_194_305])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3])
+def test_pool_past_the_one_pass_segment(V, kind):
+    """Vocabularies above 64 segments of 16384: each segment is longer than
+    one register load and is selected sub-block by sub-block with its running
+    list carried (pools and the batched top-K against the oracle)."""
+    x = adversarial_rows(2, V, V + kind)
+    ids, vals = gpu_pool(x)
+    tk_ids, tk_vals = gpu_topk(x, 16)
+    for r in range(2):
+        ref_ids, ref_vals = ov.target_pool(x[r])
+        assert np.array_equal(ids[r], ref_ids), r
+        assert np.array_equal(vals[r].view(np.uint32), ref_vals.view(np.uint32)), r
+        assert np.array_equal(tk_ids[r], ref_ids[:16]), r
+        assert np.array_equal(tk_vals[r].view(np.uint32), ref_vals[:16].view(np.uint32)), r
+
+
 def test_pool_of_the_tree_rows():
     x = adversarial_rows(25, 151936, 8)
     ids, _ = gpu_pool(x)
