@@ -147,10 +147,18 @@ VR_API int vr_workspace_bytes(int rows, int hidden, int vocab, size_t* out_bytes
  *     planes (16 significant bits, error below 2^-17 |a|); weights stream once
  *     per group.  For many rows (batched serving), where the tensor pipe sets
  *     the pace.
- *   VR_PATH_FFMA: CUDA-core FMAs, rows in passes of up to 8.
+ *   VR_PATH_FFMA: CUDA-core FMAs, rows in passes of up to 8; a pass keeps
+ *     its activations in shared memory (4 * hidden bytes per row), so hidden
+ *     above 51200 returns VR_ERR_UNSUPPORTED on this path.
  * For a given path, hidden and vocab, the bits of row r do not depend on
  * `rows` or on the other rows' values, so a row computed inside an R-row
  * call is identical to the same row computed alone.
+ * Accuracy against exact arithmetic: |error| <= 1e-3 * max(1, |logit|) on
+ * every path for hidden up to 32768, and on VR_PATH_TC up to 65536 (the
+ * tensor-core paths' fp32 accumulation error grows about linearly with
+ * hidden; VR_PATH_TC_BATCH adds both planes in one accumulator and reaches
+ * about 1.35 times that bound at 65536; VR_PATH_FFMA stays about a hundred
+ * times below it).
  * rows in [1, VR_MAX_ROWS]; hidden a multiple of 8 in [8, 65536];
  * vocab in [1, 2^31 - 1].  path: VR_PATH_*.  Writes logits only.
  */

@@ -527,3 +527,37 @@ def test_batched_call_isolates_a_request_with_invalid_data(seed):
             continue
         assert list(keep[b]["out"].cpu().numpy()[:n_em]) == ref.emitted, b
         assert int(keep[b]["acc"].item()) == ref.accept, b
+
+
+@pytest.mark.parametrize("H,path", [(16384, p) for p in PATHS] +
+                         [(65536, vb.VR_PATH_TC), (32768, vb.VR_PATH_TC_BATCH)])
+def test_wide_hidden_windows(H, path):
+    """Hidden sizes far past the test workloads' (256 K blocks at 16384, the
+    ABI's maximum 65536 on the default path): a sampled 5-row chain's window
+    against the oracle stage by stage.  The tensor-core paths' logit error
+    grows about linearly with hidden (fp32 accumulation over thousands of
+    MMA steps); the batched path, whose two planes share one accumulator,
+    stays within the tolerance up to 32768 (0.56 of the bound there, 1.35 at
+    65536, measured), the default path up to 65536 (0.67)."""
+    V, k = 1000, 4
+    W = synth.weights(V, H, seed=H + 1)
+    A = synth.activations(k + 1, H, H + 2)
+    L64 = ov.project(W, A)
+    pools = [ov.target_pool(L64[r].astype(np.float32)) for r in range(k + 1)]
+    tokens = np.array([int(pools[r][0][r % 3]) for r in range(k)], np.int32)
+    pol = ov.Policy(temperature=0.7, top_k=20, min_p=0.05, top_p=0.95)
+    win = tw.run_window(dev_weight(W), A, tokens, pol, 5, 6, path=path)
+    tw.check_window(win, L64, tokens, pol, 5, 6)
+
+
+def test_cuda_core_path_rejects_hidden_past_its_shared_memory():
+    """The CUDA-core projection keeps a pass's activations in shared memory
+    (4 * hidden bytes per row): at hidden 65536 not even one row fits, and
+    the call says so instead of running."""
+    V, H = 64, 65536
+    W = synth.weights(V, H, seed=3)
+    lg = torch.empty((1, V), dtype=torch.float32, device="cuda")
+    with pytest.raises(vb.VerifyRowError) as e:
+        vb.verify_project(dev_weight(W), dev(synth.activations(1, H, 4)), lg,
+                          vb.workspace(1, H, V), path=vb.VR_PATH_FFMA)
+    assert e.value.status == vb.VR_ERR_UNSUPPORTED
