@@ -561,3 +561,51 @@ def test_cuda_core_path_rejects_hidden_past_its_shared_memory():
         vb.verify_project(dev_weight(W), dev(synth.activations(1, H, 4)), lg,
                           vb.workspace(1, H, V), path=vb.VR_PATH_FFMA)
     assert e.value.status == vb.VR_ERR_UNSUPPORTED
+
+
+def test_host_threads_run_windows_at_once():
+    """Four host threads, each on its own stream with its own buffers and
+    workspaces, run random windows through the device and the host-buffer
+    entry points at the same time (the foreign calls release the
+    interpreter's lock): every result equals the one computed alone."""
+    import threading
+    cases = [_case(s) for s in range(700, 716)]
+    alone = []
+    for c in cases:
+        w = tw.run_window(dev_weight(c["W"]), c["A"], c["tokens"], c["pol"], c["seed"],
+                          c["position"], parent=c["parent"], q_ids=c["q_ids"], q_log=c["q_log"],
+                          hist=c["hist"], path=c["path"], separate_pen=False)
+        alone.append((w["accept"], w["n"], list(w["ids"][:w["n"]])))
+    results, errors = {}, []
+
+    def worker(t):
+        try:
+            stream = torch.cuda.Stream()
+            opt = lambda x: None if x is None or len(x) == 0 else torch.from_numpy(
+                np.ascontiguousarray(x)).pin_memory()
+            with torch.cuda.stream(stream):
+                for i in range(t, len(cases), 4):
+                    c = cases[i]
+                    R, H = c["A"].shape
+                    V = c["W"].shape[0]
+                    wd = dev_weight(c["W"])
+                    lg = torch.empty((R, V), dtype=torch.float32, device="cuda")
+                    out = torch.full((R,), -7, dtype=torch.int32).pin_memory()
+                    ws = vb.workspace(R, H, V, stream=stream)
+                    acc, n = vb.verify_window_host(
+                        wd, opt(c["A"]), opt(c["tokens"]), tw.bpol(c["pol"]), c["seed"],
+                        c["position"], lg, out, ws, parent_h=opt(c["parent"]),
+                        q_ids_h=opt(c["q_ids"]), q_logits_h=opt(c["q_log"]),
+                        hist_h=opt(c["hist"]), path=c["path"], stream=stream)
+                    results[i] = (acc, n, list(out.numpy()[:n]))
+        except Exception as e:                  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i, want in enumerate(alone):
+        assert results[i] == want, i
